@@ -1,0 +1,334 @@
+/*
+ * CSA forward-path oracle: plain, slow, fp64 CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The product path
+ * (the CUDA library and its Python binding) never calls it, and the two
+ * share no code: no headers, helpers, tables or constants.
+ *
+ * What it computes, step by step, in the order the pages describe it:
+ *   - compressed cu_seqlens (per-segment floor(len / cmp_ratio));
+ *   - the segment-clamped sliding window of original-KV rows;
+ *   - lightning-indexer scores over the causally visible compressed blocks
+ *     of the token's own segment, and their top-k;
+ *   - shared-KV MLA attention over window rows plus selected compressed
+ *     rows, with a per-head attention sink.
+ * Every floating-point input arrives as double (bf16 inputs are widened
+ * exactly by the caller); every sum, exp and log is done in double.
+ *
+ * Index convention: all row indices are stream-absolute (rows of the packed
+ * stream, not per-sample rows), as in the miles PR 2038 report, review notes
+ * ("top-k indices become stream-absolute" under THD).
+ *
+ * Parity pins: every function here is pinned by the not-gpu tests against
+ * closed forms, worked values, brute force and an independent NumPy dense
+ * oracle (see tests/test_oracle_*.py). Nothing here is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define REF_OK 0
+#define REF_ERR_ARG 1
+#define REF_ERR_NOMEM 2
+
+int csa_ref_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* cu_seqlens must start at 0 and never decrease. */
+static int check_cu(const int32_t *cu, int32_t batch, int64_t total) {
+    if (!cu || batch < 0) return 0;
+    if (cu[0] != 0) return 0;
+    for (int32_t b = 0; b < batch; ++b)
+        if (cu[b + 1] < cu[b]) return 0;
+    if (total >= 0 && cu[batch] != total) return 0;
+    return 1;
+}
+
+/* The segment that owns packed row t: the b with cu[b] <= t < cu[b+1]. */
+static int32_t segment_of(const int32_t *cu, int32_t batch, int32_t t) {
+    for (int32_t b = 0; b < batch; ++b)
+        if (t >= cu[b] && t < cu[b + 1]) return b;
+    return -1;
+}
+
+/*
+ * Compressed cu_seqlens.
+ * miles PR 2038 report, compressor.py _forward_thd docstring: the last
+ * len % cmp_ratio tokens of a segment produce no compressed entry; and
+ * "风险与影响" (risks), item 2, the same tail rule. A segment of length L
+ * therefore owns floor(L / cmp_ratio) compressed rows, and the compressed
+ * stream is packed segment after segment like the original one.
+ */
+int csa_ref_compress_cu_seqlens(const int32_t *cu_seqlens, int32_t batch, int32_t cmp_ratio,
+                                int32_t *cu_seqlens_cmp) {
+    if (!cu_seqlens || !cu_seqlens_cmp || batch < 0 || cmp_ratio < 1) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, -1)) return REF_ERR_ARG;
+    cu_seqlens_cmp[0] = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        int32_t len = cu_seqlens[b + 1] - cu_seqlens[b];
+        cu_seqlens_cmp[b + 1] = cu_seqlens_cmp[b] + len / cmp_ratio;
+    }
+    return REF_OK;
+}
+
+/*
+ * Sliding-window rows of the original KV.
+ * miles PR 2038 report, thd_utils.py get_window_topk_idxs_thd: the window of
+ * a token holds the window_size most recent rows of its own segment, self
+ * included; it is clamped to the segment start (not to stream row 0, the
+ * bug the report's motivation section lists first). Output [T, W] with the
+ * rows in ascending order from the clamped start, and -1 in every slot that
+ * would lie after the token itself.
+ * W = ori_win_left + 1 (the sparse_flash_mla schema of the hyper-parallel
+ * RFC, section 2, has ori_win_left=127, ori_win_right=0: 127 rows to the left
+ * plus the token itself).
+ */
+int csa_ref_window_idx(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
+                       int32_t ori_win_left, int32_t *idx) {
+    if (!cu_seqlens || !idx || batch < 0 || total_tokens < 0 || ori_win_left < 0) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, total_tokens)) return REF_ERR_ARG;
+    const int32_t W = ori_win_left + 1;
+    for (int32_t t = 0; t < total_tokens; ++t) {
+        int32_t b = segment_of(cu_seqlens, batch, t);
+        int32_t seg_start = cu_seqlens[b];
+        int32_t start = t - W + 1;
+        if (start < seg_start) start = seg_start;
+        for (int32_t i = 0; i < W; ++i) {
+            int32_t row = start + i;
+            idx[(int64_t)t * W + i] = (row > t) ? -1 : row;
+        }
+    }
+    return REF_OK;
+}
+
+/*
+ * Visibility of compressed block j (a stream-absolute compressed row) to
+ * token t of segment b.
+ * Block j_local of segment b pools tokens cu[b] + j_local*r ... + r - 1
+ * (miles PR 2038 report, compressor.py _forward_thd, gather_idx), so it is
+ * complete once the token at local position (j_local+1)*r - 1 has been seen.
+ * Reading (the pages fix only "causal" via cmp_mask_mode=3 in the
+ * sparse_flash_mla schema and "own segment only" via the report's fourth
+ * THD bug): visible iff j is in t's segment and (j_local+1)*r <= pos+1.
+ */
+static int block_visible(const int32_t *cu, const int32_t *cu_c, int32_t b, int32_t t,
+                         int32_t r, int32_t j) {
+    if (j < cu_c[b] || j >= cu_c[b + 1]) return 0;
+    int64_t j_local = j - cu_c[b];
+    int64_t pos = t - cu[b];
+    return (j_local + 1) * (int64_t)r <= pos + 1;
+}
+
+typedef struct {
+    double s;
+    int32_t j;
+} cand_t;
+
+/* Order: higher score first; on equal scores the lower block index first. */
+static int cand_cmp(const void *a, const void *b) {
+    const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+static int cand_cmp_j(const void *a, const void *b) {
+    const cand_t *x = (const cand_t *)a, *y = (const cand_t *)b;
+    return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+/*
+ * Lightning-indexer scores and top-k for a list of tokens.
+ * hyper-parallel RFC, section 1 (lightning_indexer schema: q, k, w, topk,
+ * cu_seqlens_q, cu_seqlens_k, cmp_ratio, return_value) and background item 1
+ * (indexer over compressed KV); miles PR 2038 report, motivation item 4
+ * (score only the query's own segment).
+ * Score (reading; the pages print no formula):
+ *     s(t, j) = sum_h w[t,h] * max(0, q[t,h,:] . k[j,:])
+ * over the visible blocks j only. Selection: the topk highest scores, ties to
+ * the lower j; fewer than topk visible -> all of them; output ascending in j,
+ * padded with -1 (and -inf values).
+ *
+ * Rows of q / w / topk_idx / topk_val / kth / next are per listed token:
+ * row i belongs to token tokens[i] (tokens == NULL: row i is token i and
+ * n_tokens must equal T). kth[i] is the topk-th best score and next[i] the
+ * (topk+1)-th (NaN when they do not exist), for judging near-ties.
+ */
+int csa_ref_indexer_topk(const double *q, const double *k, const double *w, int32_t T, int32_t Tc,
+                         int32_t Hi, int32_t Di, const int32_t *cu_seqlens,
+                         const int32_t *cu_seqlens_cmp, int32_t batch, int32_t cmp_ratio,
+                         int32_t topk, const int32_t *tokens, int32_t n_tokens, int32_t *topk_idx,
+                         double *topk_val, double *kth, double *next, int32_t *n_visible) {
+    if (!q || !w || !cu_seqlens || !cu_seqlens_cmp || !topk_idx) return REF_ERR_ARG;
+    if (Tc > 0 && !k) return REF_ERR_ARG;
+    if (T < 0 || Tc < 0 || Hi < 1 || Di < 1 || cmp_ratio < 1 || topk < 1 || n_tokens < 0) return REF_ERR_ARG;
+    if (!tokens && n_tokens != T) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, T)) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens_cmp, batch, Tc)) return REF_ERR_ARG;
+    int err = REF_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        int32_t t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) {
+            err = REF_ERR_ARG;
+            continue;
+        }
+        int32_t b = segment_of(cu_seqlens, batch, t);
+        int32_t nseg = cu_seqlens_cmp[b + 1] - cu_seqlens_cmp[b];
+        cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(nseg > 0 ? nseg : 1));
+        if (!c) {
+            err = REF_ERR_NOMEM;
+            continue;
+        }
+        int32_t n = 0;
+        for (int32_t j = cu_seqlens_cmp[b]; j < cu_seqlens_cmp[b + 1]; ++j) {
+            if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
+            double s = 0.0;
+            for (int32_t h = 0; h < Hi; ++h) {
+                const double *qh = q + ((int64_t)i * Hi + h) * Di;
+                const double *kj = k + (int64_t)j * Di;
+                double dot = 0.0;
+                for (int32_t d = 0; d < Di; ++d) dot += qh[d] * kj[d];
+                double relu = dot > 0.0 ? dot : 0.0;
+                s += w[(int64_t)i * Hi + h] * relu;
+            }
+            c[n].s = s;
+            c[n].j = j;
+            ++n;
+        }
+        qsort(c, (size_t)n, sizeof(cand_t), cand_cmp);
+        if (kth) kth[i] = (n >= topk) ? c[topk - 1].s : NAN;
+        if (next) next[i] = (n > topk) ? c[topk].s : NAN;
+        if (n_visible) n_visible[i] = n;
+        int32_t m = n < topk ? n : topk;
+        qsort(c, (size_t)m, sizeof(cand_t), cand_cmp_j);
+        for (int32_t s = 0; s < topk; ++s) {
+            topk_idx[(int64_t)i * topk + s] = s < m ? c[s].j : -1;
+            if (topk_val) topk_val[(int64_t)i * topk + s] = s < m ? c[s].s : -INFINITY;
+        }
+        free(c);
+    }
+    return err;
+}
+
+/*
+ * Shared-KV MLA sparse attention forward with attention sinks.
+ * hyper-parallel RFC, background item 2 (ori_kv band/sliding-window branch
+ * plus cmp_kv compressed branch plus attention sink) and section 2
+ * (sparse_flash_mla schema: q, ori_kv, cmp_kv, cmp_sparse_indices,
+ * cu_seqlens_q/ori_kv/cmp_kv, sinks, softmax_scale, cmp_ratio, ori_win_left,
+ * ori_win_right, return_softmax_lse); "missing arguments" analysis: the band
+ * is derived from the window arguments and ori_sparse_indices is ignored.
+ * Megatron-LM PR 7 (verl), environment note: head_dim = d_v = 512, so the
+ * whole row is both key and value.
+ *
+ * For token t and head h, with keys = the window rows of ori_kv (as
+ * csa_ref_window_idx) followed by the compressed rows of cmp_kv that are
+ * listed in cmp_sparse_indices[t] (or, when it is NULL, every visible block:
+ * the compressor-only / HCA mode), skipping -1 and any entry that is out of
+ * range or not visible to t:
+ *     l_i = softmax_scale * q[t,h,:] . kv_i
+ *     m   = max(max_i l_i, sink_h)
+ *     Z   = sum_i exp(l_i - m) + exp(sink_h - m)
+ *     out[t,h,:] = sum_i exp(l_i - m) kv_i / Z
+ *     lse[t,h]   = m + log(Z)
+ * Readings: the sink is one logit per head, not multiplied by softmax_scale,
+ * and adds to the denominator only (sinks == NULL: no sink term, which equals
+ * a sink of -inf). lse is the natural log of the full denominator including
+ * the sink, in scaled-logit units.
+ *
+ * Rows of q, cmp_sparse_indices, out and lse are per listed token as in
+ * csa_ref_indexer_topk; ori_kv and cmp_kv are the full tensors.
+ */
+int csa_ref_sparse_mla_fwd(const double *q, const double *ori_kv, const double *cmp_kv,
+                           const int32_t *cmp_sparse_indices, const int32_t *cu_seqlens,
+                           const int32_t *cu_seqlens_cmp, int32_t batch, int32_t T, int32_t Tc,
+                           int32_t H, int32_t D, int32_t topk, const double *sinks,
+                           double softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
+                           const int32_t *tokens, int32_t n_tokens, double *out, double *lse) {
+    if (!q || !ori_kv || !cu_seqlens || !out) return REF_ERR_ARG;
+    if (T < 0 || Tc < 0 || H < 1 || D < 1 || ori_win_left < 0 || n_tokens < 0) return REF_ERR_ARG;
+    if (!tokens && n_tokens != T) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, T)) return REF_ERR_ARG;
+    const int use_cmp = cmp_kv != NULL && Tc > 0;
+    if (use_cmp) {
+        if (!cu_seqlens_cmp || cmp_ratio < 1) return REF_ERR_ARG;
+        if (!check_cu(cu_seqlens_cmp, batch, Tc)) return REF_ERR_ARG;
+        if (cmp_sparse_indices && topk < 1) return REF_ERR_ARG;
+    }
+    const int32_t W = ori_win_left + 1;
+    const int32_t max_cmp = use_cmp ? (cmp_sparse_indices ? topk : Tc) : 0;
+    int err = REF_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        int32_t t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) {
+            err = REF_ERR_ARG;
+            continue;
+        }
+        int32_t b = segment_of(cu_seqlens, batch, t);
+        const double **rows = (const double **)malloc(sizeof(double *) * (size_t)(W + max_cmp));
+        double *logit = (double *)malloc(sizeof(double) * (size_t)(W + max_cmp));
+        if (!rows || !logit) {
+            free(rows);
+            free(logit);
+            err = REF_ERR_NOMEM;
+            continue;
+        }
+        int32_t n = 0;
+        /* window branch: the most recent W rows of the own segment, self included */
+        int32_t start = t - W + 1;
+        if (start < cu_seqlens[b]) start = cu_seqlens[b];
+        for (int32_t row = start; row <= t; ++row) rows[n++] = ori_kv + (int64_t)row * D;
+        /* compressed branch */
+        if (use_cmp) {
+            if (cmp_sparse_indices) {
+                for (int32_t s = 0; s < topk; ++s) {
+                    int32_t j = cmp_sparse_indices[(int64_t)i * topk + s];
+                    if (j < 0 || j >= Tc) continue;
+                    if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
+                    rows[n++] = cmp_kv + (int64_t)j * D;
+                }
+            } else {
+                for (int32_t j = cu_seqlens_cmp[b]; j < cu_seqlens_cmp[b + 1]; ++j)
+                    if (block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j))
+                        rows[n++] = cmp_kv + (int64_t)j * D;
+            }
+        }
+        for (int32_t h = 0; h < H; ++h) {
+            const double *qh = q + ((int64_t)i * H + h) * D;
+            double m = -INFINITY;
+            for (int32_t a = 0; a < n; ++a) {
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += qh[d] * rows[a][d];
+                logit[a] = softmax_scale * dot;
+                if (logit[a] > m) m = logit[a];
+            }
+            double sink = sinks ? sinks[h] : -INFINITY;
+            if (sink > m) m = sink;
+            double z = 0.0;
+            for (int32_t a = 0; a < n; ++a) z += exp(logit[a] - m);
+            if (sinks && sink != -INFINITY) z += exp(sink - m);
+            double *oh = out + ((int64_t)i * H + h) * D;
+            for (int32_t d = 0; d < D; ++d) oh[d] = 0.0;
+            for (int32_t a = 0; a < n; ++a) {
+                double p = exp(logit[a] - m) / z;
+                for (int32_t d = 0; d < D; ++d) oh[d] += p * rows[a][d];
+            }
+            if (lse) lse[(int64_t)i * H + h] = m + log(z);
+        }
+        free(rows);
+        free(logit);
+    }
+    return err;
+}
