@@ -1,0 +1,197 @@
+/*
+ * csa.h -- C ABI of the GB300 (sm_103a) forward path of DeepSeek-V4
+ * Compressed Sparse Attention (CSA) and its compressor-only mode (HCA) over
+ * THD-packed variable-length sequences, on one GPU.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [miles#2038]  "PR #2038 完整报告" (radixark/miles): "Enable THD
+ *                 packed-sequence training for DeepSeek-V4-Flash, with context
+ *                 parallelism"; sections 功能与动机 (motivation), 关键源码片段
+ *                 (key source excerpts: thd_utils.py, compressor.py), 风险与影响.
+ *   [hp#RFC]      "【RFC】DeepSeek-V4 CSA/HCA 自定义算子接入与对外接口对标
+ *                 torch_extension" (hyper-parallel); sections 背景 (background),
+ *                 1 npu_lightning_indexer, 2 npu_sparse_flash_mla, 缺失入参的用途分析
+ *                 (analysis of the missing arguments).
+ *   [MS#4842]     MindSpeed-LLM PR 4842; section 主要改动 (main changes):
+ *                 LayerCompressMode {NO_COMPRESS, COMPRESSOR_ONLY, INDEXER}.
+ *   [MLM#7]       "feat(deepseek_v4): faithful THD context-parallel path for DS4
+ *                 CSA" (verl Megatron-LM PR 7); section Environment note:
+ *                 head_dim = d_v = 512.
+ *
+ * Conventions shared by every call
+ *   - Layout is THD ("TND"): tokens of all sequences concatenated along the
+ *     first axis; cu_seqlens[batch+1] (int32, device memory, starting at 0,
+ *     non-decreasing) holds the sequence starts, as in [miles#2038] ThdLayout.
+ *     Every tensor is row-major and contiguous.
+ *   - Row indices (window rows, compressed rows, top-k output) are
+ *     stream-absolute rows of the packed tensors ([miles#2038], review notes).
+ *   - bf16 tensors are passed as csa_bf16_t (the raw 16-bit bfloat16 pattern).
+ *   - All pointers are DEVICE pointers unless stated otherwise; all sizes are
+ *     host integers. The caller owns and allocates every buffer, including
+ *     workspaces; the library allocates no device memory per call and never
+ *     synchronises the stream.
+ *   - Every call is asynchronous and stream-ordered on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream).
+ *   - Argument checks that need only host values run synchronously: a call
+ *     that returns anything but CSA_OK has launched nothing. Checks that would
+ *     need device data (cu_seqlens contents) are not made; kernels never read
+ *     or write outside the extents the host sizes imply, whatever the device
+ *     data holds, and record an inconsistency they meet in a device error word
+ *     read by csa_device_error().
+ */
+#ifndef CSA_GB300_H_
+#define CSA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *csa_stream_t;
+
+/* Raw bfloat16 bit pattern. */
+typedef uint16_t csa_bf16_t;
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_NULL = 1,         /* a required pointer is NULL                       */
+    CSA_ERR_SHAPE = 2,        /* sizes are negative or inconsistent               */
+    CSA_ERR_UNSUPPORTED = 3,  /* a valid request this build does not implement   */
+    CSA_ERR_WORKSPACE = 4,    /* workspace too small or misaligned                */
+    CSA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed      */
+    CSA_ERR_DEVICE_CHECK = 6, /* a kernel met inconsistent device data            */
+    CSA_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up               */
+} csa_status_t;
+
+/* Static string for a status code (never NULL). */
+const char *csa_status_string(csa_status_t status);
+
+/*
+ * Compressed cu_seqlens.            [miles#2038] compressor.py _forward_thd
+ * docstring and 风险与影响 item 2: the trailing len % cmp_ratio tokens of a
+ * sequence produce no compressed row, so sequence b owns floor(len_b/cmp_ratio)
+ * rows of the compressed stream:
+ *     cu_seqlens_cmp[0] = 0,
+ *     cu_seqlens_cmp[b+1] = cu_seqlens_cmp[b] + floor(len_b / cmp_ratio).
+ * cu_seqlens      [batch+1] int32 in.
+ * cu_seqlens_cmp  [batch+1] int32 out (may not alias cu_seqlens).
+ * Errors: NULL pointer -> CSA_ERR_NULL; batch < 0 -> CSA_ERR_SHAPE;
+ * cmp_ratio < 1 -> CSA_ERR_UNSUPPORTED. batch == 0 writes cu_seqlens_cmp[0]=0.
+ */
+csa_status_t csa_compress_cu_seqlens(const int32_t *cu_seqlens, int32_t batch, int32_t cmp_ratio,
+                                     int32_t *cu_seqlens_cmp, csa_stream_t stream);
+
+/*
+ * Segment-clamped sliding-window rows.   [miles#2038] thd_utils.py
+ * get_window_topk_idxs_thd; [hp#RFC] section 2 (ori_win_left=127,
+ * ori_win_right=0 defaults; band mask ori_mask_mode=4).
+ * With W = ori_win_left + 1 and token t in sequence b:
+ *     start = max(t - W + 1, cu_seqlens[b]);
+ *     idx[t, i] = start + i  if start + i <= t  else -1     (0 <= i < W)
+ * i.e. the W most recent rows of t's own sequence, self included, ascending,
+ * -1 padded at the tail.
+ * cu_seqlens [batch+1] int32 in (cu_seqlens[batch] must equal total_tokens).
+ * idx        [total_tokens, W] int32 out.
+ * Errors: NULL -> CSA_ERR_NULL; negative sizes -> CSA_ERR_SHAPE;
+ * ori_win_right != 0 -> CSA_ERR_UNSUPPORTED (only the causal band exists).
+ * total_tokens == 0 launches nothing. A token not covered by cu_seqlens
+ * (inconsistent device data) gets an all -1 row and sets the device error.
+ */
+csa_status_t csa_window_idx(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
+                            int32_t ori_win_left, int32_t ori_win_right, int32_t *idx,
+                            csa_stream_t stream);
+
+/*
+ * Bytes of device workspace csa_indexer_topk needs for these sizes
+ * (0 when it needs none). The value depends on host sizes only.
+ */
+size_t csa_indexer_topk_workspace_size(int32_t total_tokens, int32_t total_cmp, int32_t index_heads,
+                                       int32_t index_dim, int32_t topk);
+
+/*
+ * Lightning-indexer score + per-sequence causal top-k over compressed KV.
+ * [hp#RFC] section 1 (lightning_indexer(q, k, w, topk, cu_seqlens_q,
+ * cu_seqlens_k, cmp_ratio, return_value)) and background item 1;
+ * [miles#2038] 功能与动机 item 4 (score only the query's own sequence).
+ * Score of token t for compressed row j (the pages give no formula; reading):
+ *     s(t, j) = sum_h w[t,h] * max(0, q[t,h,:] . k[j,:])      (fp32 accumulate)
+ * taken over the rows j visible to t: j in t's own sequence b and
+ *     (j - cu_seqlens_cmp[b] + 1) * cmp_ratio <= (t - cu_seqlens_q[b]) + 1,
+ * i.e. the compressed row is complete (its last pooled token is at or
+ * before t). Output per token: the topk highest-scoring visible rows, ties
+ * to the lower row, emitted in ascending row order; fewer than topk visible
+ * -> all of them, then -1 (topk_val: -inf) padding.
+ * q        [T, Hi, Di] bf16      k  [Tc, Di] bf16        w [T, Hi] fp32
+ * cu_seqlens_q [batch+1], cu_seqlens_cmp_kv [batch+1] int32 (the latter as
+ *          produced by csa_compress_cu_seqlens with the same cmp_ratio).
+ * topk_idx [T, topk] int32 out; topk_val [T, topk] fp32 out or NULL.
+ * workspace: device buffer of at least csa_indexer_topk_workspace_size(...)
+ *          bytes, 256-byte aligned (may be NULL when that size is 0).
+ * Errors: NULL -> CSA_ERR_NULL (k may be NULL only when Tc == 0);
+ * negative sizes or topk < 1 -> CSA_ERR_SHAPE; Di not in {64, 128},
+ * Hi not in [1, 64], cmp_ratio < 2 -> CSA_ERR_UNSUPPORTED; workspace too
+ * small -> CSA_ERR_WORKSPACE. Tc == 0 fills topk_idx with -1.
+ */
+csa_status_t csa_indexer_topk(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                              int32_t total_tokens, int32_t total_cmp, int32_t index_heads,
+                              int32_t index_dim, const int32_t *cu_seqlens_q,
+                              const int32_t *cu_seqlens_cmp_kv, int32_t batch, int32_t cmp_ratio,
+                              int32_t topk, int32_t *topk_idx, float *topk_val, void *workspace,
+                              size_t workspace_bytes, csa_stream_t stream);
+
+/*
+ * Shared-KV MLA sparse attention forward with attention sinks.
+ * [hp#RFC] background item 2 (ori_kv band / sliding-window branch + cmp_kv
+ * compressed branch + attention sink) and section 2 (sparse_flash_mla
+ * schema; ori_sparse_indices takes no part: the band comes from the window
+ * arguments); [MLM#7] environment note (head_dim = d_v = 512: the whole
+ * 512-wide row is both key and value); [MS#4842] LayerCompressMode.
+ * For token t, head h, keys = the window rows of ori_kv (as csa_window_idx)
+ * followed by the compressed rows listed in cmp_sparse_indices[t] (entries
+ * that are -1, out of [0, Tc) or not visible to t are skipped), or, when
+ * cmp_sparse_indices is NULL, every compressed row visible to t
+ * (COMPRESSOR_ONLY / HCA mode); cmp_kv == NULL or Tc == 0 means window only:
+ *     l_i = softmax_scale * q[t,h,:] . kv_i
+ *     m   = max(max_i l_i, sink_h)
+ *     Z   = sum_i exp(l_i - m) + exp(sink_h - m)
+ *     out[t,h,:] = sum_i exp(l_i - m) kv_i / Z              (bf16, RNE)
+ *     lse[t,h]   = m + ln Z                                  (fp32)
+ * The sink is one logit per head, not scaled by softmax_scale; sinks == NULL
+ * is the same as every sink being -inf.
+ * q [T, H, D] bf16; ori_kv [T, D] bf16; cmp_kv [Tc, D] bf16 or NULL;
+ * cmp_sparse_indices [T, topk] int32 or NULL; cu_seqlens_* [batch+1] int32;
+ * sinks [H] fp32 or NULL; out [T, H, D] bf16; softmax_lse [T, H] fp32,
+ * written only when return_softmax_lse != 0 (may be NULL otherwise).
+ * Errors: NULL q/ori_kv/cu_seqlens_q/out -> CSA_ERR_NULL (cu_seqlens_cmp_kv
+ * is required when cmp_kv is used); negative sizes -> CSA_ERR_SHAPE;
+ * D != 512, H not in [1, 64], ori_win_right != 0, ori_win_left > 1023,
+ * cmp_ratio < 2 while cmp_kv is used, or cu_seqlens_ori_kv neither NULL nor
+ * equal to cu_seqlens_q (prefix KV) -> CSA_ERR_UNSUPPORTED.
+ */
+csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
+                                const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_ori_kv,
+                                const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                int32_t total_tokens, int32_t total_cmp, int32_t heads,
+                                int32_t head_dim, int32_t topk, const float *sinks,
+                                float softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
+                                int32_t ori_win_right, csa_bf16_t *out, float *softmax_lse,
+                                int32_t return_softmax_lse, csa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word of the
+ * current device: CSA_OK, CSA_ERR_DEVICE_CHECK or CSA_ERR_TIMEOUT.
+ * `detail` (host pointer, may be NULL) receives the raw word (kernel id and
+ * site in the high bits, 0 when clean).
+ */
+csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_GB300_H_ */

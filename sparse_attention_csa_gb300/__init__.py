@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) forward path of DeepSeek-V4 Compressed Sparse Attention.
+
+Thin Python binding of the C ABI declared in ``include/csa.h`` (same call
+names). It only marshals arguments: every step of the path runs in the CUDA
+kernels of ``libcsa_gb300.so``; there is no CPU or PyTorch fallback, and a
+call fails loudly when the library has not been built.
+
+PyTorch supplies device memory and the current CUDA stream. All tensors are
+CUDA tensors in THD layout, contiguous, with the dtypes ``include/csa.h``
+states (bf16 activations, fp32 weights/sinks/outputs, int32 indices).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+__all__ = [
+    "CsaError", "lib", "library_path", "csa_status_string", "csa_compress_cu_seqlens",
+    "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
+    "csa_sparse_mla_fwd", "csa_device_error", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "_build", "libcsa_gb300.so")
+
+# Every entry point include/csa.h declares.
+EXPORTED_SYMBOLS = (
+    "csa_status_string", "csa_compress_cu_seqlens", "csa_window_idx",
+    "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
+    "csa_device_error",
+)
+
+_STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
+           4: "CSA_ERR_WORKSPACE", 5: "CSA_ERR_CUDA", 6: "CSA_ERR_DEVICE_CHECK",
+           7: "CSA_ERR_TIMEOUT"}
+
+
+class CsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {csa_status_string(code)}")
+
+
+_lib = None
+_vp, _i32, _sz, _f32 = C.c_void_p, C.c_int32, C.c_size_t, C.c_float
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(
+                f"{library_path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = C.CDLL(library_path)
+        L.csa_status_string.restype = C.c_char_p
+        L.csa_status_string.argtypes = [C.c_int]
+        L.csa_compress_cu_seqlens.argtypes = [_vp, _i32, _i32, _vp, _vp]
+        L.csa_window_idx.argtypes = [_vp, _i32, _i32, _i32, _i32, _vp, _vp]
+        L.csa_indexer_topk_workspace_size.restype = _sz
+        L.csa_indexer_topk_workspace_size.argtypes = [_i32] * 5
+        L.csa_indexer_topk.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _i32, _i32,
+                                       _i32, _vp, _vp, _vp, _sz, _vp]
+        L.csa_sparse_mla_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                         _i32, _i32, _vp, _f32, _i32, _i32, _i32, _vp, _vp, _i32,
+                                         _vp]
+        L.csa_device_error.argtypes = [_vp, C.POINTER(_i32)]
+        for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
+                     "csa_sparse_mla_fwd", "csa_device_error"):
+            getattr(L, name).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def csa_status_string(code: int) -> str:
+    try:
+        return lib().csa_status_string(int(code)).decode()
+    except RuntimeError:
+        return _STATUS.get(int(code), "unknown")
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype, ndim=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise CsaError(rc, where)
+
+
+def csa_compress_cu_seqlens(cu_seqlens, cmp_ratio: int, out=None, stream=None):
+    """cu_seqlens_cmp[b+1] = cu_seqlens_cmp[b] + floor(len_b / cmp_ratio)."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(cu_seqlens)
+    _need(out, "out", torch.int32, 1)
+    _check(lib().csa_compress_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(cmp_ratio),
+                                         _ptr(out), _stream(stream)), "csa_compress_cu_seqlens")
+    return out
+
+
+def csa_window_idx(cu_seqlens, total_tokens: int, ori_win_left: int, ori_win_right: int = 0,
+                   out=None, stream=None):
+    """[T, ori_win_left+1] int32 window rows (stream-absolute, -1 padded)."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if out is None:
+        out = torch.empty((total_tokens, ori_win_left + 1), dtype=torch.int32,
+                          device=cu_seqlens.device)
+    _need(out, "out", torch.int32, 2)
+    _check(lib().csa_window_idx(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(total_tokens),
+                                int(ori_win_left), int(ori_win_right), _ptr(out), _stream(stream)),
+           "csa_window_idx")
+    return out
+
+
+def csa_indexer_topk_workspace_size(total_tokens, total_cmp, index_heads, index_dim, topk) -> int:
+    return int(lib().csa_indexer_topk_workspace_size(int(total_tokens), int(total_cmp),
+                                                     int(index_heads), int(index_dim), int(topk)))
+
+
+def csa_indexer_topk(q, k, w, cu_seqlens_q, cu_seqlens_cmp_kv, cmp_ratio: int, topk: int,
+                     return_value: bool = False, workspace=None, out=None, out_val=None,
+                     stream=None):
+    """Top-k compressed rows per token by lightning-indexer score.
+
+    Returns ``(topk_idx [T, topk] int32, topk_val [T, topk] fp32 or None)``."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_cmp_kv, "cu_seqlens_cmp_kv", torch.int32, 1)
+    T, Hi, Di = q.shape
+    Tc = 0 if k is None else k.shape[0]
+    if out is None:
+        out = torch.empty((T, topk), dtype=torch.int32, device=q.device)
+    if return_value and out_val is None:
+        out_val = torch.empty((T, topk), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.int32, 2)
+    _need(out_val, "out_val", torch.float32, 2)
+    need = csa_indexer_topk_workspace_size(T, Tc, Hi, Di, topk)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().csa_indexer_topk(
+        _ptr(q), _ptr(k) if Tc else None, _ptr(w), T, Tc, Hi, Di, _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_cmp_kv), cu_seqlens_q.numel() - 1, int(cmp_ratio), int(topk), _ptr(out),
+        _ptr(out_val) if return_value else None, _ptr(workspace), ws_bytes, _stream(stream)),
+        "csa_indexer_topk")
+    return out, (out_val if return_value else None)
+
+
+def csa_sparse_mla_fwd(q, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens_q, cu_seqlens_ori_kv,
+                       cu_seqlens_cmp_kv, sinks, softmax_scale: float, cmp_ratio: int,
+                       ori_win_left: int, ori_win_right: int = 0,
+                       return_softmax_lse: bool = False, out=None, lse=None, stream=None):
+    """Shared-KV MLA sparse attention with sinks.
+
+    ``cmp_sparse_indices`` None attends every visible compressed row (HCA);
+    ``cmp_kv`` None attends the window only. Returns ``(out, lse or None)``."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(ori_kv, "ori_kv", torch.bfloat16, 2)
+    _need(cmp_kv, "cmp_kv", torch.bfloat16, 2)
+    _need(cmp_sparse_indices, "cmp_sparse_indices", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_ori_kv, "cu_seqlens_ori_kv", torch.int32, 1)
+    _need(cu_seqlens_cmp_kv, "cu_seqlens_cmp_kv", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    T, H, D = q.shape
+    Tc = 0 if cmp_kv is None else cmp_kv.shape[0]
+    topk = 0 if cmp_sparse_indices is None else cmp_sparse_indices.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _check(lib().csa_sparse_mla_fwd(
+        _ptr(q), _ptr(ori_kv), _ptr(cmp_kv) if Tc else None, _ptr(cmp_sparse_indices),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_ori_kv), _ptr(cu_seqlens_cmp_kv),
+        cu_seqlens_q.numel() - 1, T, Tc, H, D, topk, _ptr(sinks), float(softmax_scale),
+        int(cmp_ratio), int(ori_win_left), int(ori_win_right), _ptr(out),
+        _ptr(lse) if return_softmax_lse else None, 1 if return_softmax_lse else 0,
+        _stream(stream)), "csa_sparse_mla_fwd")
+    return out, (lse if return_softmax_lse else None)
+
+
+def csa_device_error(stream=None):
+    """Synchronise the stream; return (status, raw word) of the device error word."""
+    detail = _i32(0)
+    rc = lib().csa_device_error(_stream(stream), C.byref(detail))
+    return int(rc), int(detail.value)

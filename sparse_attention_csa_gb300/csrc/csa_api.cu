@@ -1,0 +1,199 @@
+// C ABI of the CSA forward path: host-side argument checks and launches.
+// The operations, their sources on the pages and the error behaviour are
+// documented in include/csa.h.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "csa.h"
+#include "internal.h"
+
+namespace {
+
+// Device error word (one per device that loads the library).
+__device__ int32_t g_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+int32_t *g_error_ptr[kMaxDevices] = {};
+
+// Device address of g_error_word on the current device (looked up once per
+// device; cudaGetSymbolAddress is the host-side way to name it).
+int32_t *error_word(csa_status_t *st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *st = CSA_ERR_CUDA;
+        return nullptr;
+    }
+    if (!g_error_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+            *st = CSA_ERR_CUDA;
+            return nullptr;
+        }
+        g_error_ptr[dev] = static_cast<int32_t *>(p);
+    }
+    *st = CSA_OK;
+    return g_error_ptr[dev];
+}
+
+csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *csa_status_string(csa_status_t status) {
+    switch (status) {
+        case CSA_OK: return "CSA_OK";
+        case CSA_ERR_NULL: return "CSA_ERR_NULL: a required pointer is NULL";
+        case CSA_ERR_SHAPE: return "CSA_ERR_SHAPE: negative or inconsistent sizes";
+        case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: request outside what this build implements";
+        case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: workspace too small or misaligned";
+        case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA call or launch failed";
+        case CSA_ERR_DEVICE_CHECK: return "CSA_ERR_DEVICE_CHECK: a kernel met inconsistent device data";
+        case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT: a bounded device-side wait gave up";
+    }
+    return "unknown csa_status_t";
+}
+
+csa_status_t csa_compress_cu_seqlens(const int32_t *cu_seqlens, int32_t batch, int32_t cmp_ratio,
+                                     int32_t *cu_seqlens_cmp, csa_stream_t stream) {
+    if (!cu_seqlens || !cu_seqlens_cmp) return CSA_ERR_NULL;
+    if (batch < 0) return CSA_ERR_SHAPE;
+    if (cmp_ratio < 1) return CSA_ERR_UNSUPPORTED;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    return from_cuda(csa::launch_compress_cu_seqlens(cu_seqlens, batch, cmp_ratio, cu_seqlens_cmp,
+                                                     err, (cudaStream_t)stream));
+}
+
+csa_status_t csa_window_idx(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
+                            int32_t ori_win_left, int32_t ori_win_right, int32_t *idx,
+                            csa_stream_t stream) {
+    if (!cu_seqlens || !idx) return CSA_ERR_NULL;
+    if (batch < 0 || total_tokens < 0 || ori_win_left < 0) return CSA_ERR_SHAPE;
+    if (ori_win_right != 0) return CSA_ERR_UNSUPPORTED;
+    if (ori_win_left >= INT32_MAX - 1) return CSA_ERR_SHAPE;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    return from_cuda(csa::launch_window_idx(cu_seqlens, batch, total_tokens, ori_win_left + 1, idx,
+                                            err, (cudaStream_t)stream));
+}
+
+size_t csa_indexer_topk_workspace_size(int32_t total_tokens, int32_t total_cmp, int32_t index_heads,
+                                       int32_t index_dim, int32_t topk) {
+    if (total_tokens < 0 || total_cmp < 0) return 0;
+    return csa::indexer_workspace_bytes(total_tokens, total_cmp, index_heads, index_dim, topk);
+}
+
+csa_status_t csa_indexer_topk(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                              int32_t total_tokens, int32_t total_cmp, int32_t index_heads,
+                              int32_t index_dim, const int32_t *cu_seqlens_q,
+                              const int32_t *cu_seqlens_cmp_kv, int32_t batch, int32_t cmp_ratio,
+                              int32_t topk, int32_t *topk_idx, float *topk_val, void *workspace,
+                              size_t workspace_bytes, csa_stream_t stream) {
+    if (!q || !w || !cu_seqlens_q || !cu_seqlens_cmp_kv || !topk_idx) return CSA_ERR_NULL;
+    if (total_cmp > 0 && !k) return CSA_ERR_NULL;
+    if (total_tokens < 0 || total_cmp < 0 || batch < 0 || topk < 1) return CSA_ERR_SHAPE;
+    if (index_dim != 64 && index_dim != 128) return CSA_ERR_UNSUPPORTED;
+    if (index_heads < 1 || index_heads > 64) return CSA_ERR_UNSUPPORTED;
+    if (cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    const size_t need = csa::indexer_workspace_bytes(total_tokens, total_cmp, index_heads,
+                                                     index_dim, topk);
+    if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
+        return CSA_ERR_WORKSPACE;
+    // 16-byte vector loads of q / k rows
+    if (((uintptr_t)q & 15u) || (k && ((uintptr_t)k & 15u))) return CSA_ERR_UNSUPPORTED;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    csa::IndexerArgs a;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    a.w = w;
+    a.cu_q = cu_seqlens_q;
+    a.cu_c = cu_seqlens_cmp_kv;
+    a.topk_idx = topk_idx;
+    a.topk_val = topk_val;
+    a.scratch = need > 0 ? static_cast<float *>(workspace) : nullptr;
+    a.err = err;
+    a.T = total_tokens;
+    a.Tc = total_cmp;
+    a.Hi = index_heads;
+    a.Di = index_dim;
+    a.batch = batch;
+    a.cmp_ratio = cmp_ratio;
+    a.topk = topk;
+    return from_cuda(csa::launch_indexer_topk(a, (cudaStream_t)stream));
+}
+
+csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
+                                const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_ori_kv,
+                                const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                int32_t total_tokens, int32_t total_cmp, int32_t heads,
+                                int32_t head_dim, int32_t topk, const float *sinks,
+                                float softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
+                                int32_t ori_win_right, csa_bf16_t *out, float *softmax_lse,
+                                int32_t return_softmax_lse, csa_stream_t stream) {
+    if (!q || !ori_kv || !cu_seqlens_q || !out) return CSA_ERR_NULL;
+    if (return_softmax_lse && !softmax_lse) return CSA_ERR_NULL;
+    const bool use_cmp = cmp_kv != nullptr && total_cmp > 0;
+    if (use_cmp && !cu_seqlens_cmp_kv) return CSA_ERR_NULL;
+    if (batch < 0 || total_tokens < 0 || total_cmp < 0 || heads < 1 || ori_win_left < 0)
+        return CSA_ERR_SHAPE;
+    if (use_cmp && cmp_sparse_indices && topk < 1) return CSA_ERR_SHAPE;
+    if (head_dim != 512) return CSA_ERR_UNSUPPORTED;
+    if (heads > 64) return CSA_ERR_UNSUPPORTED;
+    if (ori_win_right != 0 || ori_win_left > 1023) return CSA_ERR_UNSUPPORTED;
+    if (use_cmp && cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    if (cu_seqlens_ori_kv && cu_seqlens_ori_kv != cu_seqlens_q) return CSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)q & 15u) || ((uintptr_t)ori_kv & 15u) || ((uintptr_t)out & 15u) ||
+        (use_cmp && ((uintptr_t)cmp_kv & 15u)))
+        return CSA_ERR_UNSUPPORTED;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    csa::MlaArgs a;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.ori_kv = reinterpret_cast<const __nv_bfloat16 *>(ori_kv);
+    a.cmp_kv = use_cmp ? reinterpret_cast<const __nv_bfloat16 *>(cmp_kv) : nullptr;
+    a.cmp_idx = use_cmp ? cmp_sparse_indices : nullptr;
+    a.cu_q = cu_seqlens_q;
+    a.cu_c = use_cmp ? cu_seqlens_cmp_kv : nullptr;
+    a.sinks = sinks;
+    a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    a.lse = return_softmax_lse ? softmax_lse : nullptr;
+    a.err = err;
+    a.T = total_tokens;
+    a.Tc = use_cmp ? total_cmp : 0;
+    a.H = heads;
+    a.D = head_dim;
+    a.batch = batch;
+    a.topk = use_cmp && cmp_sparse_indices ? topk : 0;
+    a.cmp_ratio = use_cmp ? cmp_ratio : 1;
+    a.window = ori_win_left + 1;
+    a.softmax_scale = softmax_scale;
+    return from_cuda(csa::launch_sparse_mla_fwd(a, (cudaStream_t)stream));
+}
+
+csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail) {
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    if (word != 0) {
+        const int32_t zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return CSA_ERR_CUDA;
+    }
+    if (detail) *detail = word;
+    if (word == 0) return CSA_OK;
+    return ((word >> 24) == csa::kErrTimeout) ? CSA_ERR_TIMEOUT : CSA_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// Internal launchers behind the C ABI. Arguments are already validated by
+// csa_api.cu; every launcher returns the cudaError_t of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+cudaError_t launch_compress_cu_seqlens(const int32_t *cu, int32_t batch, int32_t cmp_ratio,
+                                       int32_t *cu_cmp, int32_t *err, cudaStream_t stream);
+
+cudaError_t launch_window_idx(const int32_t *cu, int32_t batch, int32_t total_tokens,
+                              int32_t window, int32_t *idx, int32_t *err, cudaStream_t stream);
+
+struct IndexerArgs {
+    const __nv_bfloat16 *q;  // [T, Hi, Di]
+    const __nv_bfloat16 *k;  // [Tc, Di]
+    const float *w;          // [T, Hi]
+    const int32_t *cu_q;     // [batch+1]
+    const int32_t *cu_c;     // [batch+1]
+    int32_t *topk_idx;       // [T, topk]
+    float *topk_val;         // [T, topk] or nullptr
+    float *scratch;          // global score scratch (see indexer_workspace_bytes) or nullptr
+    int32_t *err;
+    int32_t T, Tc, Hi, Di, batch, cmp_ratio, topk;
+};
+
+size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t Hi, int32_t Di, int32_t topk);
+cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream);
+
+struct MlaArgs {
+    const __nv_bfloat16 *q;       // [T, H, D]
+    const __nv_bfloat16 *ori_kv;  // [T, D]
+    const __nv_bfloat16 *cmp_kv;  // [Tc, D] or nullptr (window only)
+    const int32_t *cmp_idx;       // [T, topk] or nullptr (all visible)
+    const int32_t *cu_q;          // [batch+1]
+    const int32_t *cu_c;          // [batch+1] (required when cmp_kv is used)
+    const float *sinks;           // [H] or nullptr
+    __nv_bfloat16 *out;           // [T, H, D]
+    float *lse;                   // [T, H] or nullptr
+    int32_t *err;
+    int32_t T, Tc, H, D, batch, topk, cmp_ratio, window;
+    float softmax_scale;
+};
+
+cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);
+
+}  // namespace csa

@@ -1,0 +1,133 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+the header declares, and rejects bad host-side arguments before touching the
+device. Also checks that the product never reaches into the oracle."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import sparse_attention_csa_gb300 as csa
+from sparse_attention_csa_gb300 import build as csa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    csa_build.build()
+    return csa.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_symbols() == sorted(csa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in [(0, "CSA_OK"), (1, "CSA_ERR_NULL"), (3, "CSA_ERR_UNSUPPORTED"),
+                       (7, "CSA_ERR_TIMEOUT")]:
+        assert csa.csa_status_string(code).startswith(name)
+    assert csa.csa_status_string(99) == "unknown csa_status_t"
+
+
+# Synchronous checks return before any CUDA call, so they run without a GPU.
+# Dummy non-null "device pointers" are never dereferenced on these paths:
+# every call below carries at least one invalid argument, so none launches.
+P = C.c_void_p(0x1000)
+NUL = None
+
+
+def test_compress_rejects(L):
+    assert L.csa_compress_cu_seqlens(NUL, 3, 4, P, NUL) == 1
+    assert L.csa_compress_cu_seqlens(P, -1, 4, P, NUL) == 2
+    assert L.csa_compress_cu_seqlens(P, 3, 0, P, NUL) == 3
+
+
+def test_window_rejects(L):
+    assert L.csa_window_idx(P, 3, 256, 15, 0, NUL, NUL) == 1
+    assert L.csa_window_idx(P, 3, -5, 15, 0, P, NUL) == 2
+    assert L.csa_window_idx(P, 3, 256, -1, 0, P, NUL) == 2
+    assert L.csa_window_idx(P, 3, 256, 15, 1, P, NUL) == 3
+
+
+def test_indexer_rejects(L):
+    args = [P, P, P, 256, 63, 4, 64, P, P, 3, 4, 8, P, NUL, NUL, 0, NUL]
+
+    def call(**kw):
+        a = list(args)
+        names = ["q", "k", "w", "T", "Tc", "Hi", "Di", "cu", "cuc", "batch", "r", "topk", "idx",
+                 "val", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return L.csa_indexer_topk(*a)
+
+    assert call(q=NUL) == 1
+    assert call(k=NUL) == 1
+    assert call(idx=NUL) == 1
+    assert call(topk=0) == 2
+    assert call(T=-1) == 2
+    assert call(Di=96) == 3
+    assert call(Hi=65) == 3
+    assert call(r=1) == 3
+    need = L.csa_indexer_topk_workspace_size(4096, 10 ** 6, 64, 128, 512)
+    assert need > 0
+    assert call(T=4096, Tc=10 ** 6, Hi=64, Di=128, topk=512) == 4
+    assert call(T=4096, Tc=10 ** 6, Hi=64, Di=128, topk=512, ws=C.c_void_p(0x1001),
+                wsb=need) == 4  # misaligned
+
+
+def test_mla_rejects(L):
+    names = ["q", "okv", "ckv", "idx", "cuq", "cuo", "cuc", "batch", "T", "Tc", "H", "D", "topk",
+             "sinks", "scale", "r", "wl", "wr", "out", "lse", "ret", "stream"]
+    base = dict(q=P, okv=P, ckv=P, idx=P, cuq=P, cuo=NUL, cuc=P, batch=3, T=256, Tc=63, H=4, D=512,
+                topk=8, sinks=P, scale=C.c_float(0.044), r=4, wl=15, wr=0, out=P, lse=P, ret=1,
+                stream=NUL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.csa_sparse_mla_fwd(*[a[n] for n in names])
+
+    assert call(q=NUL) == 1
+    assert call(out=NUL) == 1
+    assert call(lse=NUL) == 1
+    assert call(cuc=NUL) == 1
+    assert call(H=0) == 2
+    assert call(topk=0) == 2
+    assert call(D=576) == 3
+    assert call(H=65) == 3
+    assert call(wr=1) == 3
+    assert call(wl=1024) == 3
+    assert call(r=1) == 3
+    assert call(cuo=C.c_void_p(0x2000)) == 3  # prefix-KV cu_seqlens
+    assert call(q=C.c_void_p(0x1002)) == 3  # 16-byte alignment
+
+
+def test_product_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
+                assert "csa_oracle" not in text and "csa_ref_" not in text, f
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(csa, "_lib", None)
+    monkeypatch.setattr(csa, "library_path", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        csa.lib()
