@@ -251,7 +251,7 @@ class ClockSampler:
         mx = [num(r[2]) for r in rows]
         pw = [num(r[3]) for r in rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         pmax = max(p for p in pw if not math.isnan(p)) if any(not math.isnan(p) for p in pw) else 0
         loaded = [s for s, p in zip(sm, pw) if not math.isnan(s) and p >= 0.3 * pmax] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),

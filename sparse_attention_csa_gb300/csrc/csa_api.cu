@@ -70,9 +70,10 @@ csa_status_t csa_compress_cu_seqlens(const int32_t *cu_seqlens, int32_t batch, i
 csa_status_t csa_window_idx(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
                             int32_t ori_win_left, int32_t ori_win_right, int32_t *idx,
                             csa_stream_t stream) {
-    if (!cu_seqlens || !idx) return CSA_ERR_NULL;
+    if (!cu_seqlens || (!idx && total_tokens > 0)) return CSA_ERR_NULL;
     if (batch < 0 || total_tokens < 0 || ori_win_left < 0) return CSA_ERR_SHAPE;
     if (ori_win_right != 0) return CSA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return CSA_OK;
     if (ori_win_left >= INT32_MAX - 1) return CSA_ERR_SHAPE;
     csa_status_t st;
     int32_t *err = error_word(&st);
@@ -93,12 +94,13 @@ csa_status_t csa_indexer_topk(const csa_bf16_t *q, const csa_bf16_t *k, const fl
                               const int32_t *cu_seqlens_cmp_kv, int32_t batch, int32_t cmp_ratio,
                               int32_t topk, int32_t *topk_idx, float *topk_val, void *workspace,
                               size_t workspace_bytes, csa_stream_t stream) {
-    if (!q || !w || !cu_seqlens_q || !cu_seqlens_cmp_kv || !topk_idx) return CSA_ERR_NULL;
-    if (total_cmp > 0 && !k) return CSA_ERR_NULL;
     if (total_tokens < 0 || total_cmp < 0 || batch < 0 || topk < 1) return CSA_ERR_SHAPE;
     if (index_dim != 64 && index_dim != 128) return CSA_ERR_UNSUPPORTED;
     if (index_heads < 1 || index_heads > 64) return CSA_ERR_UNSUPPORTED;
     if (cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return CSA_OK;  // nothing to do (empty buffers may be NULL)
+    if (!q || !w || !cu_seqlens_q || !cu_seqlens_cmp_kv || !topk_idx) return CSA_ERR_NULL;
+    if (total_cmp > 0 && !k) return CSA_ERR_NULL;
     const size_t need = csa::indexer_workspace_bytes(total_tokens, total_cmp, index_heads,
                                                      index_dim, topk);
     if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
@@ -137,12 +139,14 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
                                 float softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
                                 int32_t ori_win_right, csa_bf16_t *out, float *softmax_lse,
                                 int32_t return_softmax_lse, csa_stream_t stream) {
-    if (!q || !ori_kv || !cu_seqlens_q || !out) return CSA_ERR_NULL;
-    if (return_softmax_lse && !softmax_lse) return CSA_ERR_NULL;
     const bool use_cmp = cmp_kv != nullptr && total_cmp > 0;
-    if (use_cmp && !cu_seqlens_cmp_kv) return CSA_ERR_NULL;
     if (batch < 0 || total_tokens < 0 || total_cmp < 0 || heads < 1 || ori_win_left < 0)
         return CSA_ERR_SHAPE;
+    if (total_tokens > 0) {  // empty buffers may be NULL
+        if (!q || !ori_kv || !cu_seqlens_q || !out) return CSA_ERR_NULL;
+        if (return_softmax_lse && !softmax_lse) return CSA_ERR_NULL;
+        if (use_cmp && !cu_seqlens_cmp_kv) return CSA_ERR_NULL;
+    }
     if (use_cmp && cmp_sparse_indices && topk < 1) return CSA_ERR_SHAPE;
     if (head_dim != 512) return CSA_ERR_UNSUPPORTED;
     if (heads > 64) return CSA_ERR_UNSUPPORTED;
@@ -152,6 +156,7 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
     if (((uintptr_t)q & 15u) || ((uintptr_t)ori_kv & 15u) || ((uintptr_t)out & 15u) ||
         (use_cmp && ((uintptr_t)cmp_kv & 15u)))
         return CSA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return CSA_OK;
     csa_status_t st;
     int32_t *err = error_word(&st);
     if (st != CSA_OK) return st;

@@ -174,10 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_simt_kernel(MlaArgs a)
                     alpha = exp2f(m_old - m_new);
                     pv = exp2f(v - m_new);
                 }
-                // round p to bf16 once so numerator and denominator agree
-                pv = __bfloat162float(__float2bfloat16_rn(pv));
+                // the denominator sums fp32 p; P.V uses p rounded to bf16
                 const float ps = warp_sum(pv);
-                sm.p[h * kChunk + lane] = pv;
+                sm.p[h * kChunk + lane] = __bfloat162float(__float2bfloat16_rn(pv));
                 __syncwarp();
                 if (lane == 0) {
                     sm.m[h] = m_new;
