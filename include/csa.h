@@ -183,6 +183,42 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
                                 int32_t return_softmax_lse, csa_stream_t stream);
 
 /*
+ * csa_indexer_topk without a workspace, for callers that cannot allocate
+ * device memory. The pages have no counterpart to this entry point.
+ *
+ * A token whose sequence offers more visible compressed rows than the
+ * kernel keeps in shared memory spills its scores to device scratch, which
+ * csa_indexer_topk takes from the caller. A plugin that a host framework
+ * hands only its input and output buffers, or a runtime held to a memory
+ * budget fixed at start-up, may be unable to call cudaMalloc (it can
+ * synchronise the device and fragments a pool the caller does not own).
+ * This variant computes exactly what csa_indexer_topk computes, with the
+ * same arguments minus the workspace, and uses instead a scratch array of
+ * 32 MiB that lives in the library: every GPU that loads the library holds
+ * that array until the process exits. The call allocates nothing.
+ *
+ * Limits and sharing:
+ *   - total_cmp above 8,388,608 rows (one CTA's scores no longer fit in the
+ *     array) -> CSA_ERR_WORKSPACE; other errors as csa_indexer_topk.
+ *   - When scores may spill, the grid is limited to as many CTAs as the
+ *     array has slots of total_cmp floats.
+ *   - Every call shares the array and leaves its contents behind; nothing in
+ *     it needs to start at zero (each score is written before it is read).
+ *     Calls that overlap on the GPU (e.g. on two streams at once) race on
+ *     the array: order them on one stream.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up with that device current); make that first call before
+ *     any stream capture.
+ */
+csa_status_t csa_indexer_topk_noalloc(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                                      int32_t total_tokens, int32_t total_cmp,
+                                      int32_t index_heads, int32_t index_dim,
+                                      const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                      int32_t cmp_ratio, int32_t topk, int32_t *topk_idx,
+                                      float *topk_val, csa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word of the
  * current device: CSA_OK, CSA_ERR_DEVICE_CHECK or CSA_ERR_TIMEOUT.
  * `detail` (host pointer, may be NULL) receives the raw word (kernel id and

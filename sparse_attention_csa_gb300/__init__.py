@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "CsaError", "lib", "library_path", "csa_status_string", "csa_compress_cu_seqlens",
     "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
-    "csa_sparse_mla_fwd", "csa_device_error", "EXPORTED_SYMBOLS",
+    "csa_sparse_mla_fwd", "csa_device_error", "csa_indexer_topk_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ library_path = os.path.join(_HERE, "_build", "libcsa_gb300.so")
 EXPORTED_SYMBOLS = (
     "csa_status_string", "csa_compress_cu_seqlens", "csa_window_idx",
     "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
-    "csa_device_error",
+    "csa_device_error", "csa_indexer_topk_noalloc",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -69,8 +69,10 @@ def lib():
                                          _i32, _i32, _vp, _f32, _i32, _i32, _i32, _vp, _vp, _i32,
                                          _vp]
         L.csa_device_error.argtypes = [_vp, C.POINTER(_i32)]
+        L.csa_indexer_topk_noalloc.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp,
+                                               _i32, _i32, _i32, _vp, _vp, _vp]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
-                     "csa_sparse_mla_fwd", "csa_device_error"):
+                     "csa_sparse_mla_fwd", "csa_device_error", "csa_indexer_topk_noalloc"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -169,6 +171,32 @@ def csa_indexer_topk(q, k, w, cu_seqlens_q, cu_seqlens_cmp_kv, cmp_ratio: int, t
         _ptr(cu_seqlens_cmp_kv), cu_seqlens_q.numel() - 1, int(cmp_ratio), int(topk), _ptr(out),
         _ptr(out_val) if return_value else None, _ptr(workspace), ws_bytes, _stream(stream)),
         "csa_indexer_topk")
+    return out, (out_val if return_value else None)
+
+
+def csa_indexer_topk_noalloc(q, k, w, cu_seqlens_q, cu_seqlens_cmp_kv, cmp_ratio: int,
+                             topk: int, return_value: bool = False, out=None, out_val=None,
+                             stream=None):
+    """Same result as :func:`csa_indexer_topk`, for callers that cannot
+    allocate device memory: no workspace, the library's own fixed 32 MiB
+    scratch array instead (shared by every call; order calls on one stream)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_cmp_kv, "cu_seqlens_cmp_kv", torch.int32, 1)
+    T, Hi, Di = q.shape
+    Tc = 0 if k is None else k.shape[0]
+    if out is None:
+        out = torch.empty((T, topk), dtype=torch.int32, device=q.device)
+    if return_value and out_val is None:
+        out_val = torch.empty((T, topk), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.int32, 2)
+    _need(out_val, "out_val", torch.float32, 2)
+    _check(lib().csa_indexer_topk_noalloc(
+        _ptr(q), _ptr(k) if Tc else None, _ptr(w), T, Tc, Hi, Di, _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_cmp_kv), cu_seqlens_q.numel() - 1, int(cmp_ratio), int(topk), _ptr(out),
+        _ptr(out_val) if return_value else None, _stream(stream)), "csa_indexer_topk_noalloc")
     return out, (out_val if return_value else None)
 
 

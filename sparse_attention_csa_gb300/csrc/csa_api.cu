@@ -39,6 +39,10 @@ csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_E
 
 }  // namespace
 
+namespace csa {
+int32_t *device_error_word(csa_status_t *st) { return error_word(st); }
+}  // namespace csa
+
 extern "C" {
 
 const char *csa_status_string(csa_status_t status) {

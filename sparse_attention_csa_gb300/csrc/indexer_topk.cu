@@ -206,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_topk_kernel(IndexerArgs a
 
 }  // namespace
 
+int32_t indexer_scratch_rows_threshold() { return kScoreCap; }
+
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t, int32_t, int32_t) {
     if (Tc <= kScoreCap || T <= 0) return 0;
     const int64_t ctas = T < kMaxCtas ? T : kMaxCtas;
@@ -221,6 +223,7 @@ cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     int ctas = a.T < sms ? a.T : sms;
     if (ctas > kMaxCtas) ctas = kMaxCtas;
+    if (a.max_ctas > 0 && ctas > a.max_ctas) ctas = a.max_ctas;
     const size_t smem = sizeof(Smem) + (size_t)kScoreCap * sizeof(float);
     if (a.Di == 64) {
         e = cudaFuncSetAttribute(indexer_topk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "csa.h"
+
 namespace csa {
 
 cudaError_t launch_compress_cu_seqlens(const int32_t *cu, int32_t batch, int32_t cmp_ratio,
@@ -24,9 +26,14 @@ struct IndexerArgs {
     float *scratch;          // global score scratch (see indexer_workspace_bytes) or nullptr
     int32_t *err;
     int32_t T, Tc, Hi, Di, batch, cmp_ratio, topk;
+    int32_t max_ctas = 0;    // grid bound when > 0 (scratch sized for that many CTAs)
 };
 
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t Hi, int32_t Di, int32_t topk);
+// A token whose sequence offers more visible compressed rows than this keeps
+// its scores in the scratch (one slot of Tc floats per CTA) instead of
+// shared memory.
+int32_t indexer_scratch_rows_threshold();
 cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream);
 
 struct MlaArgs {
@@ -45,5 +52,8 @@ struct MlaArgs {
 };
 
 cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);
+
+// Device error word of the current device (csa_api.cu).
+int32_t *device_error_word(csa_status_t *st);
 
 }  // namespace csa
