@@ -156,6 +156,8 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
     if (heads > 64) return CSA_ERR_UNSUPPORTED;
     if (ori_win_right != 0 || ori_win_left > 1023) return CSA_ERR_UNSUPPORTED;
     if (use_cmp && cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    if (use_cmp && cmp_sparse_indices && topk > csa::sparse_mla_max_topk())
+        return CSA_ERR_UNSUPPORTED;
     if (cu_seqlens_ori_kv && cu_seqlens_ori_kv != cu_seqlens_q) return CSA_ERR_UNSUPPORTED;
     if (((uintptr_t)q & 15u) || ((uintptr_t)ori_kv & 15u) || ((uintptr_t)out & 15u) ||
         (use_cmp && ((uintptr_t)cmp_kv & 15u)))

@@ -52,6 +52,8 @@ struct MlaArgs {
 };
 
 cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);
+// Largest topk (entries of cmp_sparse_indices per token) the kernel accepts.
+int32_t sparse_mla_max_topk();
 
 // Device error word of the current device (csa_api.cu).
 int32_t *device_error_word(csa_status_t *st);
