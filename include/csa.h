@@ -199,10 +199,11 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
  * that array until the process exits. The call allocates nothing.
  *
  * Limits and sharing:
- *   - total_cmp above 8,388,608 rows (one CTA's scores no longer fit in the
- *     array) -> CSA_ERR_WORKSPACE; other errors as csa_indexer_topk.
+ *   - total_cmp above 2,097,152 rows (one CTA's slot, the scores of four
+ *     tokens, no longer fits in the array) -> CSA_ERR_WORKSPACE; other
+ *     errors as csa_indexer_topk.
  *   - When scores may spill, the grid is limited to as many CTAs as the
- *     array has slots of total_cmp floats.
+ *     array has slots of 4 x total_cmp floats.
  *   - Every call shares the array and leaves its contents behind; nothing in
  *     it needs to start at zero (each score is written before it is read).
  *     Calls that overlap on the GPU (e.g. on two streams at once) race on

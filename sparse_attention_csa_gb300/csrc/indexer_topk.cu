@@ -1,4 +1,5 @@
-// Lightning-indexer score + per-sequence causal top-k over compressed KV.
+// Lightning-indexer score + per-sequence causal top-k over compressed KV
+// (sm_103a, tcgen05 tensor cores, TMA).
 //
 // Sources: hyper-parallel RFC "DeepSeek-V4 CSA/HCA 自定义算子接入…", section 1
 // (lightning_indexer schema: q, k, w, topk, cu_seqlens_q, cu_seqlens_k,
@@ -10,144 +11,182 @@
 // or before t. Top-k: ties to the lower row, output in ascending row order,
 // -1 / -inf padding.
 //
-// One CTA owns one token at a time (persistent grid). Scores live in shared
-// memory (global scratch beyond kScoreCap candidates); the K-th largest is
-// found by a 4-pass 8-bit radix select on order-preserving uint32 keys, and
-// the winners are emitted in row order with two block scans.
+// Design (persistent grid, 1 CTA per SM):
+//   * Four consecutive tokens form a group. The contraction is done with the
+//     compressed rows on the MMA's M side and the group's (token, head) pairs
+//     on N:   S^T[j, (g,h)] = k[j, :] . q[t0+g, h, :]
+//     (M = 128 rows, N = 4 x Hpad <= 256, K = Di), accumulated in fp32 in
+//     tensor memory, double-buffered (2 x 256 columns) so the epilogue of one
+//     tile overlaps the MMA of the next. With one TMEM lane per row j, the head
+//     reduction sum_h w*relu(.) runs inside each thread.
+//   * A group whose tokens span several sequences is processed as one pass per
+//     sequence (each with its own row range); visibility masks per token.
+//   * Scores of the group stay in shared memory (global scratch when a
+//     sequence offers more than kScoreCap rows); afterwards each of the four
+//     epilogue warps selects one token's top-k with a warp-level 4-pass 8-bit
+//     radix select on order-preserving keys and emits the winners in row
+//     order with warp scans.
+//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
+//     and selection. Every mbarrier wait is bounded.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace csa {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kScoreCap = 40960;        // candidates kept in shared memory
-constexpr int kMaxCtas = 1024;          // persistent grid bound (sizes the scratch)
-constexpr int kMaxHi = 64, kMaxDi = 128;
+constexpr int kThreads = 192;
+constexpr int kG = 4;               // tokens per group
+constexpr int kTileRows = 128;      // compressed rows per MMA tile
+constexpr int kScoreCap = 5120;     // rows per token kept in shared memory
+constexpr int kMaxCtas = 1024;      // persistent grid bound (sizes the scratch)
 
-struct Smem {
-    float q[kMaxHi * kMaxDi];
-    float w[kMaxHi];
-    int32_t hist[256];
-    int32_t scan[kThreads / 32 + 1];
-    uint32_t sel_digit;
-    int32_t sel_above;
+// shared memory map (1024-aligned base)
+constexpr uint32_t kOffB = 0;                 // q group: 2 chunks x [256 rows x 128 B]
+constexpr uint32_t kOffA = 65536;             // k tiles: 2 stages x 2 chunks x 16 KB
+constexpr uint32_t kOffScore = 131072;        // kG x kScoreCap fp32
+constexpr uint32_t kOffMisc = kOffScore + kG * kScoreCap * 4;
+
+struct Pass {
+    int32_t mask, cbase, n_tiles, pad;
 };
 
-template <int DI>
-__device__ __forceinline__ float score_row(const Smem &sm, const __nv_bfloat16 *__restrict__ krow,
-                                           int hi) {
-    // row of k in registers (bf16 pairs), q broadcast from shared memory
-    __nv_bfloat162 kr[DI / 2];
-    const uint4 *src = reinterpret_cast<const uint4 *>(krow);
-#pragma unroll
-    for (int v = 0; v < DI / 8; ++v) {
-        uint4 x = __ldg(src + v);
-        kr[4 * v + 0] = *reinterpret_cast<__nv_bfloat162 *>(&x.x);
-        kr[4 * v + 1] = *reinterpret_cast<__nv_bfloat162 *>(&x.y);
-        kr[4 * v + 2] = *reinterpret_cast<__nv_bfloat162 *>(&x.z);
-        kr[4 * v + 3] = *reinterpret_cast<__nv_bfloat162 *>(&x.w);
-    }
-    float s = 0.0f;
-    for (int h = 0; h < hi; ++h) {
-        const float2 *qh = reinterpret_cast<const float2 *>(sm.q + h * DI);
-        float dot = 0.0f;
-#pragma unroll
-        for (int p = 0; p < DI / 2; ++p) {
-            float2 qq = qh[p];
-            float2 kk = __bfloat1622float2(kr[p]);
-            dot = fmaf(qq.x, kk.x, dot);
-            dot = fmaf(qq.y, kk.y, dot);
-        }
-        s = fmaf(sm.w[h], fmaxf(dot, 0.0f), s);
-    }
-    return s;
+struct GroupInfo {
+    int32_t t0, n_pass, spill, valid;
+    int32_t nv[kG];       // visible rows per token (0: none / out of range)
+    int32_t cb[kG];       // row base of each token's sequence
+    Pass pass[kG];
+};
+
+struct Misc {
+    uint64_t b_full, b_empty;
+    uint64_t a_full[2], a_empty[2];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t info_full[2], info_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+    GroupInfo info[2];
+    float w[kG * 64];
+    int32_t hist[4][256];
+};
+
+constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+
+__device__ __forceinline__ bool bar_red_and(bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v)
+        : "memory");
+    return out != 0;
 }
 
-// Returns the exact key of the K-th largest element (radix select, MSB first)
-// and, through *take_eq, how many elements equal to it belong to the top K.
-__device__ uint32_t radix_select(Smem &sm, const float *sc, int32_t n, int32_t K,
-                                 int32_t *take_eq) {
-    uint32_t prefix = 0, mask = 0;
-    int32_t k_rem = K;
-    const int lane = threadIdx.x & 31;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = threadIdx.x; i < 256; i += kThreads) sm.hist[i] = 0;
-        __syncthreads();
-        for (int32_t i = threadIdx.x; i < n; i += kThreads) {
-            uint32_t u = float_key(sc[i]);
-            if ((u & mask) == prefix) atomicAdd(&sm.hist[(u >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            // lane L holds digits 255-8L .. 248-8L (descending)
-            int32_t c[8], local = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = sm.hist[255 - (lane * 8 + i)];
-                local += c[i];
-            }
-            int32_t incl = local;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            int32_t above = incl - local;  // elements with a larger digit than this lane's first
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (above < k_rem && k_rem <= above + c[i]) {
-                    sm.sel_digit = 255u - (uint32_t)(lane * 8 + i);
-                    sm.sel_above = above;
-                }
-                above += c[i];
-            }
-        }
-        __syncthreads();
-        const uint32_t d = sm.sel_digit;
-        k_rem -= sm.sel_above;
-        prefix |= d << shift;
-        mask |= 255u << shift;
-        __syncthreads();
+struct Ctx {
+    Misc *m;
+    int32_t *err;
+    __device__ __forceinline__ bool aborted() const {
+        return *reinterpret_cast<volatile int32_t *>(&m->abort) != 0;
     }
-    *take_eq = k_rem;
-    return prefix;
+    __device__ __forceinline__ void fail(int site) const {
+        *reinterpret_cast<volatile int32_t *>(&m->abort) = 1;
+        report_error(err, kErrTimeout, kKerIndexer, site);
+    }
+    __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, int site) const {
+        if (aborted()) return false;
+        if (tc::mbar_wait(bar, parity)) return true;
+        fail(site);
+        return false;
+    }
+};
+
+__device__ __forceinline__ int32_t warp_excl_scan(int32_t v, int lane, int32_t *total) {
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
 }
 
-// Writes the selected rows of one token in ascending order.
-__device__ void emit_topk(Smem &sm, const float *sc, int32_t n, int32_t K, int32_t base,
-                          int32_t *__restrict__ idx_row, float *__restrict__ val_row) {
+// One warp selects the top K of sc[0..n) (ties to the lower index) and writes
+// them in ascending index order as base + index (values alongside).
+__device__ void warp_topk(const float *sc, int32_t n, int32_t K, int32_t base,
+                          int32_t *__restrict__ idx_row, float *__restrict__ val_row,
+                          int32_t *hist, int lane) {
     if (n <= K) {
-        for (int32_t i = threadIdx.x; i < K; i += kThreads) {
+        for (int32_t i = lane; i < K; i += 32) {
             idx_row[i] = i < n ? base + i : -1;
             if (val_row) val_row[i] = i < n ? sc[i] : -INFINITY;
         }
         return;
     }
-    int32_t take_eq;
-    const uint32_t tau = radix_select(sm, sc, n, K, &take_eq);
-    const int32_t per = (n + kThreads - 1) / kThreads;
-    const int32_t c0 = min(n, (int32_t)threadIdx.x * per), c1 = min(n, c0 + per);
+    uint32_t prefix = 0, mask = 0;
+    int32_t k_rem = K;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hist[lane + 32 * i] = 0;
+        __syncwarp();
+        for (int32_t i = lane; i < n; i += 32) {
+            const uint32_t u = float_key(sc[i]);
+            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+        }
+        __syncwarp();
+        int32_t c[8], local = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = hist[255 - (lane * 8 + i)];
+            local += c[i];
+        }
+        int32_t tot;
+        int32_t above = warp_excl_scan(local, lane, &tot);
+        int32_t my_digit = -1, my_above = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (above < k_rem && k_rem <= above + c[i]) {
+                my_digit = 255 - (lane * 8 + i);
+                my_above = above;
+            }
+            above += c[i];
+        }
+        const uint32_t who = __ballot_sync(0xffffffffu, my_digit >= 0);
+        const int src = who ? __ffs(who) - 1 : 0;
+        const int32_t digit = __shfl_sync(0xffffffffu, my_digit, src);
+        k_rem -= __shfl_sync(0xffffffffu, my_above, src);
+        prefix |= (uint32_t)max(digit, 0) << shift;
+        mask |= 255u << shift;
+        __syncwarp();
+    }
+    const uint32_t tau = prefix;
+    const int32_t per = (n + 31) / 32;
+    const int32_t c0 = min(n, lane * per), c1 = min(n, c0 + per);
     int32_t gt = 0, eq = 0;
     for (int32_t i = c0; i < c1; ++i) {
-        uint32_t u = float_key(sc[i]);
+        const uint32_t u = float_key(sc[i]);
         gt += u > tau;
         eq += u == tau;
     }
-    int32_t total;
-    const int32_t eq_before = block_exclusive_scan<kThreads>(eq, sm.scan, &total);
-    const int32_t my_eq = max(0, min(eq, take_eq - eq_before));
-    int32_t pos = block_exclusive_scan<kThreads>(gt + my_eq, sm.scan, &total);
-    int32_t eq_seen = 0;
+    int32_t tot;
+    const int32_t eq_before = warp_excl_scan(eq, lane, &tot);
+    const int32_t my_eq = max(0, min(eq, k_rem - eq_before));
+    int32_t pos = warp_excl_scan(gt + my_eq, lane, &tot);
+    int32_t seen = 0;
     for (int32_t i = c0; i < c1; ++i) {
-        uint32_t u = float_key(sc[i]);
+        const uint32_t u = float_key(sc[i]);
         bool take = u > tau;
         if (u == tau) {
-            take = eq_seen < my_eq;
-            ++eq_seen;
+            take = seen < my_eq;
+            ++seen;
         }
         if (take && pos < K) {  // exactly K are taken; the bound only guards the row
             idx_row[pos] = base + i;
@@ -157,50 +196,314 @@ __device__ void emit_topk(Smem &sm, const float *sc, int32_t n, int32_t K, int32
     }
 }
 
+template <int HPAD, int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+                  const __grid_constant__ CUtensorMap k_map, const __grid_constant__ IndexerArgs a) {
+    constexpr int N = kG * HPAD;          // MMA N
+    constexpr int NCH = DI / 64;          // 128-byte chunks per row
+    constexpr uint32_t kBChunk = N * 128; // bytes per B chunk
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~uintptr_t(1023));
+    Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx cx{ms, a.err};
+    const int32_t n_groups = (a.T + kG - 1) / kG;
+
+    if (tid == 0) {
+        tc::mbar_init(&ms->b_full, 1);
+        tc::mbar_init(&ms->b_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&ms->a_full[i], 1);
+            tc::mbar_init(&ms->a_empty[i], 1);
+            tc::mbar_init(&ms->acc_full[i], 1);
+            tc::mbar_init(&ms->acc_empty[i], 128);
+            tc::mbar_init(&ms->info_full[i], 1);
+            tc::mbar_init(&ms->info_empty[i], 5);
+        }
+        tc::mbar_init(&ms->drain, 1);
+        ms->abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&ms->tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch_desc(&q_map);
+        tc::tma_prefetch_desc(&k_map);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = ms->tmem_base;
+
+    if (warp == 0) {
+        // ===================================================== producer warp
+        uint32_t it = 0, b_n = 0, a_n = 0;
+        for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+            GroupInfo gi;
+            gi.t0 = grp * kG;
+            gi.n_pass = 0;
+            gi.spill = 0;
+            gi.valid = 1;
+            int32_t segs[kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                const int32_t t = gi.t0 + g;
+                gi.nv[g] = 0;
+                gi.cb[g] = 0;
+                gi.pass[g] = Pass{0, 0, 0, 0};
+                segs[g] = -1;
+                if (t >= a.T) continue;
+                const int32_t b = find_segment(a.cu_q, a.batch, t);
+                if (b < 0) {
+                    if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 1);
+                    continue;
+                }
+                segs[g] = b;
+                if (a.Tc == 0) continue;
+                const int32_t pos = t - __ldg(a.cu_q + b);
+                const int32_t cbase = __ldg(a.cu_c + b);
+                int32_t nv = min((pos + 1) / a.cmp_ratio, __ldg(a.cu_c + b + 1) - cbase);
+                if (cbase < 0 || nv < 0 || (int64_t)cbase + nv > a.Tc) {
+                    if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 2);
+                    nv = 0;
+                }
+                gi.nv[g] = nv;
+                gi.cb[g] = cbase;
+                if (nv > kScoreCap) gi.spill = 1;
+            }
+            // one pass per run of tokens sharing a sequence
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                if (segs[g] < 0 || gi.nv[g] == 0) continue;
+                const bool joins = g > 0 && gi.n_pass > 0 && segs[g - 1] == segs[g] &&
+                                   gi.nv[g - 1] > 0;
+                if (joins) {
+                    Pass &p = gi.pass[gi.n_pass - 1];
+                    p.mask |= 1 << g;
+                    p.n_tiles = max(p.n_tiles, (gi.nv[g] + kTileRows - 1) / kTileRows);
+                } else {
+                    Pass &p = gi.pass[gi.n_pass++];
+                    p.mask = 1 << g;
+                    p.cbase = gi.cb[g];
+                    p.n_tiles = (gi.nv[g] + kTileRows - 1) / kTileRows;
+                    p.pad = 0;
+                }
+            }
+            if (gi.spill && a.scratch == nullptr) {
+                if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 3);
+                gi.valid = 0;
+            }
+            const uint32_t slot = it & 1;
+            bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) {
+                ms->info[slot] = gi;
+                tc::mbar_arrive(&ms->info_full[slot]);
+            }
+            if (!gi.valid || gi.n_pass == 0) continue;
+            // q rows of the group (4 tokens x HPAD heads; missing rows read as 0)
+            ok = cx.wait(&ms->b_empty, (b_n & 1) ^ 1, 11);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) {
+                tc::mbar_expect_tx(&ms->b_full, NCH * kBChunk);
+                for (int c = 0; c < NCH; ++c)
+                    tc::tma_load_3d(smem + kOffB + c * kBChunk, &q_map, &ms->b_full, 64 * c, 0,
+                                    gi.t0);
+            }
+            ++b_n;
+            bool broke = false;
+            for (int p = 0; p < gi.n_pass && !broke; ++p) {
+                for (int32_t j = 0; j < gi.pass[p].n_tiles; ++j, ++a_n) {
+                    const uint32_t st = a_n & 1;
+                    ok = cx.wait(&ms->a_empty[st], ((a_n >> 1) & 1) ^ 1, 12);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        broke = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc::mbar_expect_tx(&ms->a_full[st], NCH * 16384u);
+                        for (int c = 0; c < NCH; ++c)
+                            tc::tma_load_2d(smem + kOffA + st * 32768 + c * 16384, &k_map,
+                                            &ms->a_full[st], 64 * c,
+                                            gi.pass[p].cbase + j * kTileRows);
+                    }
+                }
+            }
+            if (broke) break;
+        }
+        // drain: every copy issued has landed before the CTA exits
+        if (lane == 0) {
+            if (b_n > 0 && !tc::mbar_wait(&ms->b_full, (b_n - 1) & 1)) cx.fail(13);
+            for (uint32_t k = (a_n > 2 ? a_n - 2 : 0); k < a_n; ++k)
+                if (!tc::mbar_wait(&ms->a_full[k & 1], (k >> 1) & 1)) cx.fail(14);
+        }
+    } else if (warp == 1) {
+        // ========================================================= MMA warp
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(128, N, false, false);
+            const uint32_t a_base = tc::smem_u32(smem + kOffA);
+            const uint32_t b_base = tc::smem_u32(smem + kOffB);
+            uint32_t it = 0, b_n = 0, a_n = 0, t_n = 0;
+            bool issued = false;
+            for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+                const uint32_t slot = it & 1;
+                if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
+                const GroupInfo gi = ms->info[slot];
+                tc::mbar_arrive(&ms->info_empty[slot]);
+                if (!gi.valid || gi.n_pass == 0) continue;
+                if (!cx.wait(&ms->b_full, b_n & 1, 21)) break;
+                ++b_n;
+                bool stop = false;
+                for (int p = 0; p < gi.n_pass && !stop; ++p) {
+                    for (int32_t j = 0; j < gi.pass[p].n_tiles; ++j, ++a_n, ++t_n) {
+                        const uint32_t st = a_n & 1, buf = t_n & 1;
+                        if (!cx.wait(&ms->acc_empty[buf], ((t_n >> 1) & 1) ^ 1, 22) ||
+                            !cx.wait(&ms->a_full[st], (a_n >> 1) & 1, 23)) {
+                            stop = true;
+                            break;
+                        }
+                        tc::tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < DI / 16; ++kk) {
+                            const int c = kk / 4, ks = kk % 4;
+                            tc::mma_bf16(tmem + buf * 256,
+                                         tc::smem_desc(a_base + st * 32768 + c * 16384 + ks * 32,
+                                                       16, 1024),
+                                         tc::smem_desc(b_base + c * kBChunk + ks * 32, 16, 1024),
+                                         idesc, kk > 0);
+                        }
+                        issued = true;
+                        tc::mma_commit(&ms->a_empty[st]);
+                        tc::mma_commit(&ms->acc_full[buf]);
+                    }
+                }
+                if (stop) break;
+                tc::mma_commit(&ms->b_empty);
+            }
+            if (issued) {
+                tc::mma_commit(&ms->drain);
+                if (!tc::mbar_wait(&ms->drain, 0)) cx.fail(24);
+            }
+        }
+        __syncwarp();
+    } else {
+        // =========================================== epilogue + selection
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;
+        const int ltid = tid - 64;
+        const int sel_warp = warp - 2;  // token of the group this warp selects for
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+        float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
+        uint32_t it = 0, t_n = 0;
+        for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+            const uint32_t slot = it & 1;
+            bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
+            if (!bar_red_and(ok)) break;
+            // read in place; the slot is released at the end of the group
+            const GroupInfo &gi = ms->info[slot];
+            float *sc;
+            int32_t sc_stride;
+            if (gi.spill) {
+                sc = a.scratch + (int64_t)blockIdx.x * kG * a.Tc;
+                sc_stride = a.Tc;
+            } else {
+                sc = sc_smem;
+                sc_stride = kScoreCap;
+            }
+            // weights of the group's tokens (0 beyond Hi / T)
+            for (int i = ltid; i < kG * 64; i += 128) {
+                const int g = i >> 6, h = i & 63;
+                const int32_t t = gi.t0 + g;
+                ms->w[i] = (h < a.Hi && t < a.T) ? __ldg(a.w + (int64_t)t * a.Hi + h) : 0.0f;
+            }
+            tc::named_bar_sync(1, 128);
+            bool stop = false;
+            if (gi.valid) {
+                for (int p = 0; p < gi.n_pass && !stop; ++p) {
+                    const Pass &ps = gi.pass[p];
+                    for (int32_t j = 0; j < ps.n_tiles; ++j, ++t_n) {
+                        const uint32_t buf = t_n & 1;
+                        ok = cx.wait(&ms->acc_full[buf], (t_n >> 1) & 1, 31);
+                        if (!bar_red_and(ok)) {
+                            stop = true;
+                            break;
+                        }
+                        tc::tc_fence_after();
+                        float acc[kG];
+#pragma unroll
+                        for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
+#pragma unroll
+                        for (int cc = 0; cc < (N + 31) / 32; ++cc) {
+                            float x[32];
+                            tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int col = 32 * cc + i;
+                                if (col < N) {
+                                    const int g = col / HPAD, h = col % HPAD;
+                                    acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
+                                }
+                            }
+                        }
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(&ms->acc_empty[buf]);
+                        const int32_t jl = j * kTileRows + row;
+#pragma unroll
+                        for (int g = 0; g < kG; ++g)
+                            if (((ps.mask >> g) & 1) && jl < gi.nv[g])
+                                sc[(int64_t)g * sc_stride + jl] = acc[g];
+                    }
+                }
+            }
+            if (stop) break;
+            tc::named_bar_sync(1, 128);  // scores complete
+            {
+                const int g = sel_warp;
+                const int32_t t = gi.t0 + g;
+                if (t < a.T) {
+                    int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
+                    float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
+                    const int32_t n = gi.valid ? gi.nv[g] : 0;
+                    warp_topk(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row, val_row,
+                              ms->hist[sel_warp], lane);
+                }
+            }
+            tc::named_bar_sync(1, 128);  // scores free for the next group
+            if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int HPAD, int DI>
+cudaError_t launch_t(const IndexerArgs &a, const CUtensorMap &qm, const CUtensorMap &km, int ctas,
+                     cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<HPAD, DI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    indexer_tc_kernel<HPAD, DI><<<ctas, kThreads, kSmemBytes, stream>>>(qm, km, a);
+    return cudaGetLastError();
+}
+
 template <int DI>
-__global__ void __launch_bounds__(kThreads, 1) indexer_topk_kernel(IndexerArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
-    float *sc_smem = reinterpret_cast<float *>(smem_raw + sizeof(Smem));
-    for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
-        float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
-        const int32_t b = find_segment(a.cu_q, a.batch, t);
-        int32_t n = 0, base = 0;
-        if (b < 0) {
-            if (threadIdx.x == 0) report_error(a.err, kErrCheck, kKerIndexer, 1);
-        } else if (a.Tc > 0) {
-            const int32_t pos = t - __ldg(a.cu_q + b);
-            base = __ldg(a.cu_c + b);
-            const int32_t seg_blocks = __ldg(a.cu_c + b + 1) - base;
-            n = min((pos + 1) / a.cmp_ratio, seg_blocks);
-            if (base < 0 || n < 0 || base + n > a.Tc) {
-                if (threadIdx.x == 0) report_error(a.err, kErrCheck, kKerIndexer, 2);
-                n = 0;
-            }
-        }
-        if (n == 0) {
-            for (int32_t i = threadIdx.x; i < a.topk; i += kThreads) {
-                idx_row[i] = -1;
-                if (val_row) val_row[i] = -INFINITY;
-            }
-            continue;
-        }
-        float *sc = n <= kScoreCap ? sc_smem : a.scratch + (int64_t)blockIdx.x * a.Tc;
-        if (n > kScoreCap && a.scratch == nullptr) {
-            if (threadIdx.x == 0) report_error(a.err, kErrCheck, kKerIndexer, 3);
-            continue;
-        }
-        __syncthreads();  // previous token done with shared memory
-        const __nv_bfloat16 *qt = a.q + (int64_t)t * a.Hi * DI;
-        for (int i = threadIdx.x; i < a.Hi * DI; i += kThreads) sm.q[i] = __bfloat162float(qt[i]);
-        for (int i = threadIdx.x; i < a.Hi; i += kThreads) sm.w[i] = a.w[(int64_t)t * a.Hi + i];
-        __syncthreads();
-        for (int32_t j = threadIdx.x; j < n; j += kThreads)
-            sc[j] = score_row<DI>(sm, a.k + (int64_t)(base + j) * DI, a.Hi);
-        __syncthreads();
-        emit_topk(sm, sc, n, a.topk, base, idx_row, val_row);
-        __syncthreads();
+cudaError_t launch_di(const IndexerArgs &a, int hpad, const CUtensorMap &qm, const CUtensorMap &km,
+                      int ctas, cudaStream_t stream) {
+    switch (hpad) {
+        case 4: return launch_t<4, DI>(a, qm, km, ctas, stream);
+        case 8: return launch_t<8, DI>(a, qm, km, ctas, stream);
+        case 16: return launch_t<16, DI>(a, qm, km, ctas, stream);
+        case 32: return launch_t<32, DI>(a, qm, km, ctas, stream);
+        default: return launch_t<64, DI>(a, qm, km, ctas, stream);
     }
 }
 
@@ -208,10 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_topk_kernel(IndexerArgs a
 
 int32_t indexer_scratch_rows_threshold() { return kScoreCap; }
 
+int64_t indexer_scratch_floats_per_cta(int32_t Tc) { return (int64_t)kG * Tc; }
+
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t, int32_t, int32_t) {
     if (Tc <= kScoreCap || T <= 0) return 0;
-    const int64_t ctas = T < kMaxCtas ? T : kMaxCtas;
-    return (size_t)ctas * (size_t)Tc * sizeof(float);
+    const int64_t groups = ((int64_t)T + kG - 1) / kG;
+    const int64_t ctas = groups < kMaxCtas ? groups : kMaxCtas;
+    return (size_t)ctas * (size_t)indexer_scratch_floats_per_cta(Tc) * sizeof(float);
 }
 
 cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream) {
@@ -221,20 +527,22 @@ cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    int ctas = a.T < sms ? a.T : sms;
+    const int32_t groups = (a.T + kG - 1) / kG;
+    int ctas = groups < sms ? groups : sms;
     if (ctas > kMaxCtas) ctas = kMaxCtas;
     if (a.max_ctas > 0 && ctas > a.max_ctas) ctas = a.max_ctas;
-    const size_t smem = sizeof(Smem) + (size_t)kScoreCap * sizeof(float);
-    if (a.Di == 64) {
-        e = cudaFuncSetAttribute(indexer_topk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        indexer_topk_kernel<64><<<ctas, kThreads, smem, stream>>>(a);
+    const int hpad = a.Hi <= 4 ? 4 : a.Hi <= 8 ? 8 : a.Hi <= 16 ? 16 : a.Hi <= 32 ? 32 : 64;
+    CUtensorMap qm, km;
+    // q viewed as [T][Hi][Di]; a box of (64 dims, hpad heads, 4 tokens) zero-fills
+    // heads >= Hi and tokens >= T.
+    if (!encode_bf16_3d(&qm, a.q, a.Di, a.Hi, a.T, 64, hpad, kG)) return cudaErrorInvalidValue;
+    if (a.Tc > 0) {
+        if (!encode_bf16_2d(&km, a.k, a.Tc, a.Di, 64, kTileRows)) return cudaErrorInvalidValue;
     } else {
-        e = cudaFuncSetAttribute(indexer_topk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        indexer_topk_kernel<128><<<ctas, kThreads, smem, stream>>>(a);
+        km = qm;  // never read: no token has a visible row
     }
-    return cudaGetLastError();
+    return a.Di == 64 ? launch_di<64>(a, hpad, qm, km, ctas, stream)
+                      : launch_di<128>(a, hpad, qm, km, ctas, stream);
 }
 
 }  // namespace csa

@@ -34,6 +34,8 @@ size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t Hi, int32_t Di, in
 // its scores in the scratch (one slot of Tc floats per CTA) instead of
 // shared memory.
 int32_t indexer_scratch_rows_threshold();
+// Floats of scratch one CTA uses when scores spill (its slot).
+int64_t indexer_scratch_floats_per_cta(int32_t Tc);
 cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream);
 
 struct MlaArgs {

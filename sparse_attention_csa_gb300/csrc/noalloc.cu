@@ -54,8 +54,8 @@ extern "C" csa_status_t csa_indexer_topk_noalloc(
     if (index_dim != 64 && index_dim != 128) return CSA_ERR_UNSUPPORTED;
     if (index_heads < 1 || index_heads > 64) return CSA_ERR_UNSUPPORTED;
     if (cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
-    // One CTA's scores (total_cmp floats) must fit in the static scratch.
-    if ((int64_t)total_cmp > kScratchFloats) return CSA_ERR_WORKSPACE;
+    // One CTA's slot (the scores of a group of tokens) must fit in the array.
+    if (csa::indexer_scratch_floats_per_cta(total_cmp) > kScratchFloats) return CSA_ERR_WORKSPACE;
     if (total_tokens == 0) return CSA_OK;
     if (!q || !w || !cu_seqlens_q || !cu_seqlens_cmp_kv || !topk_idx) return CSA_ERR_NULL;
     if (total_cmp > 0 && !k) return CSA_ERR_NULL;
@@ -81,12 +81,12 @@ extern "C" csa_status_t csa_indexer_topk_noalloc(
     a.cmp_ratio = cmp_ratio;
     a.topk = topk;
     if (total_cmp > csa::indexer_scratch_rows_threshold()) {
-        // Scores may spill: every CTA gets its own slot of total_cmp floats,
-        // so the grid is bounded by how many slots the array holds. Nothing in
-        // the slots needs clearing: each score is written before it is read.
+        // Scores may spill: every CTA gets its own slot, so the grid is
+        // bounded by how many slots the array holds. Nothing in the slots
+        // needs clearing: each score is written before it is read.
         st = scratch_address(&a.scratch);
         if (st != CSA_OK) return st;
-        a.max_ctas = (int32_t)(kScratchFloats / total_cmp);
+        a.max_ctas = (int32_t)(kScratchFloats / csa::indexer_scratch_floats_per_cta(total_cmp));
     }
     return csa::launch_indexer_topk(a, (cudaStream_t)stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }

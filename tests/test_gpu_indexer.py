@@ -36,7 +36,8 @@ def test_tiny_pack_full():
     check_topk(case, idx, ref, gpu_val=val)
 
 
-@pytest.mark.parametrize("hi,di,k", [(64, 128, 64), (8, 64, 16), (4, 64, 1), (64, 64, 300)])
+@pytest.mark.parametrize("hi,di,k", [(64, 128, 64), (8, 64, 16), (4, 64, 1), (64, 64, 300),
+                                     (12, 128, 8), (33, 64, 40)])
 def test_medium_pack_full(hi, di, k):
     lengths = [1, 3, 700, 5, 1100, 260, 4, 9]
     layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=k, index_heads=hi, index_dim=di)

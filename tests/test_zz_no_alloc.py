@@ -56,6 +56,7 @@ def test_noalloc_matches_workspace_entry_point():
 def test_noalloc_rejects_more_rows_than_the_scratch_holds():
     L = csa.lib()
     p = C.c_void_p(0x1000)  # never dereferenced: the size check comes first
-    rc = L.csa_indexer_topk_noalloc(p, p, p, 1 << 24, (1 << 23) + 1, 4, 64, p, p, 1, 4, 8, p,
-                                    None, None)
-    assert rc == 4  # CSA_ERR_WORKSPACE
+    for rows in ((1 << 21) + 1, (1 << 23) + 1):  # one CTA slot holds 4 x rows floats
+        rc = L.csa_indexer_topk_noalloc(p, p, p, 1 << 24, rows, 4, 64, p, p, 1, 4, 8, p,
+                                        None, None)
+        assert rc == 4  # CSA_ERR_WORKSPACE
