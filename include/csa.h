@@ -169,7 +169,7 @@ csa_status_t csa_indexer_topk(const csa_bf16_t *q, const csa_bf16_t *k, const fl
  * Errors: NULL q/ori_kv/cu_seqlens_q/out -> CSA_ERR_NULL (cu_seqlens_cmp_kv
  * is required when cmp_kv is used); negative sizes -> CSA_ERR_SHAPE;
  * D != 512, H not in [1, 64], ori_win_right != 0, ori_win_left > 1023,
- * cmp_ratio < 2 while cmp_kv is used, topk > 2048 with cmp_sparse_indices,
+ * cmp_ratio < 2 while cmp_kv is used, topk > 1024 with cmp_sparse_indices,
  * or cu_seqlens_ori_kv neither NULL nor equal to cu_seqlens_q (prefix KV)
  * -> CSA_ERR_UNSUPPORTED. q, ori_kv, cmp_kv and out must be 16-byte aligned.
  */

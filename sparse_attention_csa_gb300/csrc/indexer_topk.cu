@@ -346,8 +346,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // ========================================================= MMA warp
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(128, N, false, false);
-            const uint32_t a_base = tc::smem_u32(smem + kOffA);
-            const uint32_t b_base = tc::smem_u32(smem + kOffB);
+            const uint64_t da = tc::smem_desc(tc::smem_u32(smem + kOffA), 16, 1024);
+            const uint64_t db = tc::smem_desc(tc::smem_u32(smem + kOffB), 16, 1024);
             uint32_t it = 0, b_n = 0, a_n = 0, t_n = 0;
             bool issued = false;
             for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
@@ -372,10 +372,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         for (int kk = 0; kk < DI / 16; ++kk) {
                             const int c = kk / 4, ks = kk % 4;
                             tc::mma_bf16(tmem + buf * 256,
-                                         tc::smem_desc(a_base + st * 32768 + c * 16384 + ks * 32,
-                                                       16, 1024),
-                                         tc::smem_desc(b_base + c * kBChunk + ks * 32, 16, 1024),
-                                         idesc, kk > 0);
+                                         tc::desc_add(da, st * 32768 + c * 16384 + ks * 32),
+                                         tc::desc_add(db, c * kBChunk + ks * 32), idesc, kk > 0);
                         }
                         issued = true;
                         tc::mma_commit(&ms->a_empty[st]);

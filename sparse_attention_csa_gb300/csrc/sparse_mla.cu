@@ -1,5 +1,5 @@
 // Shared-KV MLA sparse attention forward with attention sinks (sm_103a,
-// tcgen05 tensor cores, TMA).
+// tcgen05 tensor cores, TMA and cp.async).
 //
 // Sources: hyper-parallel RFC "DeepSeek-V4 CSA/HCA 自定义算子接入…", background
 // item 2 (ori_kv band/sliding-window branch + cmp_kv compressed branch +
@@ -19,18 +19,25 @@
 //     contraction is done transposed, with the keys on the MMA's M side:
 //         S^T[key, h]  = K[key, :] . Q[h, :]        M=128 keys, N=64, K=512
 //         O^T[d, h]   += V[key, d]^T P[key, h]      M=128 d (x4), N=64, K=128
-//     K and V are the same gathered rows: one 128-key x 512 tile in shared
-//     memory (SW128, K-major) serves S^T as the A operand and, read MN-major,
-//     O^T as the A operand. Accumulators live in tensor memory: S^T in 64
-//     columns, O^T in 4 x 64 columns.
-//   * Key rows are gathered by TMA gather4 (4 rows x 128 bytes per copy) from
-//     two tensor maps (ori_kv, cmp_kv). A token's key list is: its window rows,
-//     padded to a multiple of 4 (padding masked), then its valid compressed
-//     rows (compacted from cmp_sparse_indices, or the visible range).
-//   * Warp roles: warp 0 builds key lists and issues TMA, warp 1 owns tensor
-//     memory and issues tcgen05.mma (one thread), warps 2-5 run the softmax
-//     (one thread per key = one TMEM lane, 64 head scores each) and the
-//     epilogue (one thread per d row of O^T).
+//     K and V are the same rows: one 128-key x 512 tile in shared memory
+//     (SW128, K-major) serves S^T as the A operand and, read MN-major, O^T as
+//     the A operand. Accumulators live in tensor memory: S^T in 64 columns,
+//     O^T in 4 x 64 columns.
+//   * Key tiles. A token with at most 128 keys gets one tile: its window rows
+//     then its compressed rows, gathered with 16-byte cp.async. Otherwise its
+//     window rows (one contiguous run) fill tiles of their own, loaded by 2-D
+//     TMA boxes of 128 rows, and its compressed rows follow in their own
+//     tiles: by TMA boxes too when they form one ascending run (always in the
+//     compressor-only mode, and in the indexer mode whenever top-k covers
+//     every visible block) and at least half a tile long, else gathered by
+//     cp.async. Rows of a box past the tile's valid count are masked. (TMA
+//     gather4 moves single 128-byte rows an order of magnitude slower than
+//     these paths.) Q arrives by 3-D TMA.
+//   * Warp roles: 0 scheduler (key lists, Q), 1-2 loaders (K/V tiles),
+//     3 tensor memory + tcgen05.mma issue (one thread), 4-11 softmax and
+//     epilogue in two warpgroups of 32 heads each (softmax: one thread per key
+//     = one TMEM lane, 32 head scores; epilogue: one thread per d row of O^T,
+//     8 x 8 blocks transposed across lanes in registers, 16-byte stores).
 //   * Online softmax in base 2 with a lazily moved running max: a head's max
 //     only moves when a tile exceeds it by more than 8 (a factor 256), so O^T
 //     in tensor memory is rescaled rarely. Row sums accumulate per thread in
@@ -46,57 +53,93 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 384;  // 12 warps
 constexpr int kTileKeys = 128;
-constexpr int kMaxList = 2048;  // compressed indices per token (topk bound)
+constexpr int kMaxList = 1024;  // compressed indices per token (topk bound)
+constexpr int kLoaders = 64;    // threads of the two loader warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.0f;  // base-2 units
+constexpr int kMinBoxRows = 64;   // shorter compressed runs are gathered, not boxed
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffKV = 0;            // 8 chunks x [128 keys x 128 B]
 constexpr uint32_t kOffQ = 131072;        // 8 chunks x [64 heads x 128 B]
 constexpr uint32_t kOffP = 196608;        // [128 keys x 64 heads] bf16, MN-major
-constexpr uint32_t kOffList = 212992;     // kMaxList int32
-constexpr uint32_t kOffMisc = kOffList + kMaxList * 4;
+constexpr uint32_t kOffList = 212992;     // 2 x kMaxList int32 (one per token slot)
+constexpr uint32_t kOffMisc = kOffList + 2 * kMaxList * 4;
 
 // tensor memory columns
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 
+enum : int32_t { kTileOri = 0, kTileCmp = 1, kTileGather = 2 };
+enum : int32_t { kFlagMixed = 1, kFlagCmpRun = 2 };
+
 struct TokenInfo {
-    int32_t t, n_win, n_win4, n_keys, n_tiles, valid;
+    int32_t t, n_win, n_cmp, n_tiles;
+    int32_t valid, win_start, cmp_first, flags;
 };
 
+struct TileDesc {
+    int32_t kind;     // kTileOri / kTileCmp (TMA box of 128 rows from row0) or kTileGather
+    int32_t row0;     // first row of the box
+    int32_t n_valid;  // slots [0, n_valid) hold keys
+    int32_t key0;     // key index (window rows first, then compressed) of slot 0
+};
+
+__device__ __forceinline__ TileDesc tile_desc(const TokenInfo &ti, int32_t j) {
+    if (ti.flags & kFlagMixed) return {kTileGather, 0, ti.n_win + ti.n_cmp, 0};
+    const int32_t nwt = (ti.n_win + kTileKeys - 1) / kTileKeys;
+    if (j < nwt)
+        return {kTileOri, ti.win_start + j * kTileKeys, min(kTileKeys, ti.n_win - j * kTileKeys),
+                j * kTileKeys};
+    const int32_t jc = j - nwt;
+    const int32_t n = min(kTileKeys, ti.n_cmp - jc * kTileKeys);
+    if ((ti.flags & kFlagCmpRun) && n >= kMinBoxRows)
+        return {kTileCmp, ti.cmp_first + jc * kTileKeys, n, ti.n_win + jc * kTileKeys};
+    return {kTileGather, 0, n, ti.n_win + jc * kTileKeys};
+}
+
 struct Misc {
-    uint64_t q_full, q_empty;
-    uint64_t kv_full[4], kv_empty[4];
+    uint64_t q_full[4], q_empty[4];   // per pair of 64-wide chunks of Q
+    uint64_t kv_full[4], kv_empty[4]; // per slab (pair of chunks) of the K/V tile
     uint64_t s_full, p_full, o_full, drain;
     uint64_t info_full[2], info_empty[2];
     uint32_t tmem_base;
     int32_t abort;
-    int32_t rescale[2];
     TokenInfo info[2];
-    float red[4][64];
-    float m_run[64];
-    float alpha[64];
-    float inv_l[64];
+    __align__(16) float red[2][4][64];   // [tile parity][lane quarter][head]
+    __align__(16) float sink2[64];       // sink * log2(e), -inf when absent
 };
 
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ bool bar_red_and(bool v) {
+// AND of v over the 128 threads of named barrier `id`.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, bool v) {
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "r"(id)
         : "memory");
     return out != 0;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 struct Ctx {
@@ -118,97 +161,85 @@ struct Ctx {
     }
 };
 
-// 64 values per thread -> lane L holds the warp-wide reduction of heads 2L, 2L+1.
+// 32 values per thread -> lane L holds the warp-wide reduction of value L.
 template <bool kMax>
-__device__ __forceinline__ void reduce_scatter64(const float (&x)[64], float &o0, float &o1,
-                                                 int lane) {
+__device__ __forceinline__ float reduce_scatter32(const float (&x)[32], int lane) {
     auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-    float a[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const bool hi = lane & 16;
-        const float send = hi ? x[i] : x[32 + i];
-        const float keep = hi ? x[32 + i] : x[i];
-        a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-    }
     float b[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const bool hi = lane & 8;
-        const float send = hi ? a[i] : a[16 + i];
-        const float keep = hi ? a[16 + i] : a[i];
-        b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        const bool hi = lane & 16;
+        const float send = hi ? x[i] : x[16 + i];
+        const float keep = hi ? x[16 + i] : x[i];
+        b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
     }
     float c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const bool hi = lane & 4;
+        const bool hi = lane & 8;
         const float send = hi ? b[i] : b[8 + i];
         const float keep = hi ? b[8 + i] : b[i];
-        c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
     }
     float d[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const bool hi = lane & 2;
+        const bool hi = lane & 4;
         const float send = hi ? c[i] : c[4 + i];
         const float keep = hi ? c[4 + i] : c[i];
-        d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+        d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
     }
-    {
-        const bool hi = lane & 1;
-        const float s0 = hi ? d[0] : d[2], k0 = hi ? d[2] : d[0];
-        const float s1 = hi ? d[1] : d[3], k1 = hi ? d[3] : d[1];
-        o0 = op(k0, __shfl_xor_sync(0xffffffffu, s0, 1));
-        o1 = op(k1, __shfl_xor_sync(0xffffffffu, s1, 1));
+    float e[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool hi = lane & 2;
+        const float send = hi ? d[i] : d[2 + i];
+        const float keep = hi ? d[2 + i] : d[i];
+        e[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
     }
+    const bool hi = lane & 1;
+    return op(hi ? e[1] : e[0], __shfl_xor_sync(0xffffffffu, hi ? e[0] : e[1], 1));
 }
-
-struct Params {
-    MlaArgs a;
-    int32_t window;
-};
 
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ CUtensorMap ori_map,
                      const __grid_constant__ CUtensorMap cmp_map,
-                     const __grid_constant__ Params P) {
+                     const __grid_constant__ MlaArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~uintptr_t(1023));
     Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
-    int32_t *list = reinterpret_cast<int32_t *>(smem + kOffList);
-    const MlaArgs &a = P.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Ctx cx{ms, a.err};
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        tc::mbar_init(&ms->q_full, 1);
-        tc::mbar_init(&ms->q_empty, 1);
         for (int s = 0; s < 4; ++s) {
-            tc::mbar_init(&ms->kv_full[s], 1);
+            tc::mbar_init(&ms->q_full[s], 1);
+            tc::mbar_init(&ms->q_empty[s], 1);
+            tc::mbar_init(&ms->kv_full[s], kLoaders);
             tc::mbar_init(&ms->kv_empty[s], 1);
         }
         tc::mbar_init(&ms->s_full, 1);
-        tc::mbar_init(&ms->p_full, 128);
+        tc::mbar_init(&ms->p_full, 256);
         tc::mbar_init(&ms->o_full, 1);
         tc::mbar_init(&ms->drain, 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&ms->info_full[i], 1);
-            tc::mbar_init(&ms->info_empty[i], 5);
+            tc::mbar_init(&ms->info_empty[i], 11);  // MMA + 8 softmax + 2 loader warps
         }
         ms->abort = 0;
-        ms->rescale[0] = ms->rescale[1] = 0;
         tc::fence_mbar_init();
     }
+    if (tid < 64)
+        ms->sink2[tid] = (a.sinks && tid < a.H) ? __ldg(a.sinks + tid) * kLog2e : -INFINITY;
     // Rows never written by a copy must hold finite values: zero Q and KV once.
     for (uint32_t i = tid; i < (kOffP - kOffKV) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffKV)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
-    if (warp == 1) {
+    if (warp == 3) {
         tc::tmem_alloc(&ms->tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -224,24 +255,36 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     const bool use_cmp = a.cmp_kv != nullptr && a.Tc > 0;
 
     if (warp == 0) {
-        // ===================================================== producer warp
-        uint32_t it = 0, q_n = 0, kv_n = 0;
+        // ================================================== scheduler warp
+        uint32_t it = 0, q_n = 0;
+        int32_t seg_lo = 0, seg_hi = 0, seg_b = -1;  // last sequence found: [lo, hi)
         for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
-            // ---- key list of token t
-            TokenInfo ti{t, 0, 0, 0, 0, 0};
-            int32_t win_start = 0, cbase = 0;
-            const int32_t b = find_segment(a.cu_q, a.batch, t);
+            const uint32_t slot = it & 1;
+            // the slot's key list is rewritten only once every consumer is done
+            bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            int32_t *list = reinterpret_cast<int32_t *>(smem + kOffList) + slot * kMaxList;
+            TokenInfo ti{t, 0, 0, 0, 0, 0, 0, 0};
+            // tokens of a CTA increase, so the last sequence usually still holds t
+            if (seg_b < 0 || t < seg_lo || t >= seg_hi) {
+                seg_b = find_segment(a.cu_q, a.batch, t);
+                if (seg_b >= 0) {
+                    seg_lo = __ldg(a.cu_q + seg_b);
+                    seg_hi = __ldg(a.cu_q + seg_b + 1);
+                }
+            }
+            const int32_t b = seg_b;
             if (b < 0) {
                 if (lane == 0) report_error(a.err, kErrCheck, kKerMla, 1);
             } else {
-                const int32_t seg0 = max(__ldg(a.cu_q + b), 0);
+                const int32_t seg0 = max(seg_lo, 0);
                 const int32_t pos = t - seg0;
-                win_start = max(t - P.window + 1, seg0);
-                ti.n_win = t - win_start + 1;
-                ti.n_win4 = (ti.n_win + 3) & ~3;
+                ti.win_start = max(t - a.window + 1, seg0);
+                ti.n_win = t - ti.win_start + 1;
                 int32_t n_cmp = 0;
+                bool run = true;
                 if (use_cmp) {
-                    cbase = __ldg(a.cu_c + b);
+                    const int32_t cbase = __ldg(a.cu_c + b);
                     const int32_t seg_blocks = __ldg(a.cu_c + b + 1) - cbase;
                     int32_t vis = min((pos + 1) / a.cmp_ratio, seg_blocks);
                     if (cbase < 0 || vis < 0 || (int64_t)cbase + vis > a.Tc) {
@@ -249,106 +292,186 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         vis = 0;
                     }
                     if (a.cmp_idx) {
+                        // Compact the valid entries, in entry order. Each round
+                        // issues all 16 loads of 512 entries before using any.
                         const int32_t *row = a.cmp_idx + (int64_t)t * a.topk;
-                        for (int32_t e0 = 0; e0 < a.topk; e0 += 32) {
-                            const int32_t e = e0 + lane;
-                            const int32_t j = e < a.topk ? __ldg(row + e) : -1;
-                            const bool ok = j >= cbase && j < cbase + vis;
-                            const uint32_t m = __ballot_sync(0xffffffffu, ok);
-                            if (ok) list[n_cmp + __popc(m & ((1u << lane) - 1u))] = j;
-                            n_cmp += __popc(m);
+                        for (int32_t e0 = 0; e0 < a.topk; e0 += 512) {
+                            int32_t jv[16];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                const int32_t e = e0 + 32 * r + lane;
+                                jv[r] = e < a.topk ? __ldg(row + e) : -1;
+                            }
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                const bool v = jv[r] >= cbase && jv[r] < cbase + vis;
+                                const uint32_t m = __ballot_sync(0xffffffffu, v);
+                                if (v) list[n_cmp + __popc(m & ((1u << lane) - 1u))] = jv[r];
+                                n_cmp += __popc(m);
+                            }
+                        }
+                        __syncwarp();
+                        // one ascending run of consecutive rows?
+                        if (n_cmp > 0) {
+                            const int32_t first = list[0];
+                            bool mine = true;
+                            for (int32_t e = lane; e < n_cmp; e += 32) mine &= list[e] == first + e;
+                            run = __all_sync(0xffffffffu, mine);
+                            ti.cmp_first = first;
                         }
                     } else {
                         n_cmp = vis;
+                        ti.cmp_first = cbase;
                     }
                 }
-                ti.n_keys = ti.n_win4 + n_cmp;
-                ti.n_tiles = (ti.n_keys + kTileKeys - 1) / kTileKeys;
+                ti.n_cmp = n_cmp;
+                const int32_t n_keys = ti.n_win + n_cmp;
+                if (n_keys <= kTileKeys) {
+                    ti.flags = kFlagMixed;
+                    ti.n_tiles = 1;
+                } else {
+                    ti.flags = run ? kFlagCmpRun : 0;
+                    ti.n_tiles = (ti.n_win + kTileKeys - 1) / kTileKeys +
+                                 (n_cmp + kTileKeys - 1) / kTileKeys;
+                }
                 ti.valid = 1;
             }
-            __syncwarp();
-            // ---- publish the token
-            const uint32_t slot = it & 1;
-            bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            __syncwarp();  // list writes before the release below
             if (lane == 0) {
                 ms->info[slot] = ti;
                 tc::mbar_arrive(&ms->info_full[slot]);
             }
             if (!ti.valid) continue;
-            // ---- Q rows of token t (H rows of 512; rows >= H stay zero)
-            ok = cx.wait(&ms->q_empty, (q_n & 1) ^ 1, 11);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            if (lane == 0) {
-                tc::mbar_expect_tx(&ms->q_full, 8u * a.H * 128u);
-                for (int c = 0; c < 8; ++c)
-                    tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full, 64 * c, 0, t);
-            }
-            ++q_n;
-            // ---- key tiles: lane g gathers slots 4g..4g+3 of each tile
-            bool broke = false;
-            for (int32_t j = 0; j < ti.n_tiles; ++j, ++kv_n) {
-                const int32_t s0 = j * kTileKeys + 4 * lane;
-                const bool group_on = s0 < ti.n_keys;
-                const int32_t left = ti.n_keys - j * kTileKeys;
-                const int32_t n_groups = min(32, (left + 3) >> 2);
-                // Groups never straddle the window/compressed boundary
-                // (n_win4 is a multiple of 4); slots past n_keys repeat the
-                // group's last real row and are masked like the padding.
-                int32_t r[4] = {t, t, t, t};
-                bool from_cmp = false;
-                if (group_on) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int32_t s = min(s0 + e, ti.n_keys - 1);
-                        if (s < ti.n_win) {
-                            r[e] = win_start + s;
-                        } else if (s < ti.n_win4) {
-                            r[e] = t;  // window padding (masked)
-                        } else {
-                            from_cmp = true;
-                            const int32_t ci = s - ti.n_win4;
-                            r[e] = a.cmp_idx ? list[ci] : cbase + ci;
-                        }
+            // Q rows of token t (H rows of 512; rows >= H stay zero), one pair
+            // of 64-wide chunks at a time as the previous token frees them
+            bool qbroke = false;
+            for (int pr = 0; pr < 4; ++pr) {
+                ok = cx.wait(&ms->q_empty[pr], (q_n & 1) ^ 1, 11);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    qbroke = true;
+                    break;
+                }
+                if (lane == 0) {
+                    tc::mbar_expect_tx(&ms->q_full[pr], 2u * a.H * 128u);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * pr + cc;
+                        tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full[pr], 64 * c, 0,
+                                        t);
                     }
                 }
-                const CUtensorMap *map = from_cmp ? &cmp_map : &ori_map;
+            }
+            if (qbroke) break;
+            ++q_n;
+        }
+        if (lane == 0 && q_n > 0)  // drain: every Q copy issued has landed
+            for (int pr = 0; pr < 4; ++pr)
+                if (!tc::mbar_wait(&ms->q_full[pr], (q_n - 1) & 1)) cx.fail(13);
+    } else if (warp == 1 || warp == 2) {
+        // ==================================================== loader warps
+        // Gathered tiles: thread i covers, for slab s, the 16-byte column
+        // 16 s + (i & 15) of the slots k = (i >> 4) + 4 m (m < 32): one
+        // 256-byte row piece per quarter-warp, so every global access is a
+        // coalesced run. Row addresses are computed once per tile.
+        const int li = tid - 32;  // 0..63
+        const int col = li & 15, sgrp = li >> 4;
+        uint32_t it = 0, kv_n = 0;
+        const uint32_t kv_base = tc::smem_u32(smem + kOffKV);
+        bool stop = false;
+        for (int32_t t = blockIdx.x; t < a.T && !stop; t += gridDim.x, ++it) {
+            const uint32_t slot = it & 1;
+            if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40)) break;
+            const TokenInfo ti = ms->info[slot];
+            const int32_t *list = reinterpret_cast<const int32_t *>(smem + kOffList) + slot * kMaxList;
+            for (int32_t j = 0; j < ti.n_tiles && !stop; ++j, ++kv_n) {
+                const TileDesc td = tile_desc(ti, j);
+                if (td.kind != kTileGather) {
+                    const CUtensorMap *map = td.kind == kTileOri ? &ori_map : &cmp_map;
+                    for (int s = 0; s < 4; ++s) {
+                        if (!cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 41)) {
+                            stop = true;
+                            break;
+                        }
+                        if (li == 0) {
+                            tc::mbar_expect_tx(&ms->kv_full[s], 32768u);
+                            for (int cc = 0; cc < 2; ++cc) {
+                                const int c = 2 * s + cc;
+                                tc::tma_load_2d(smem + kOffKV + c * 16384, map, &ms->kv_full[s],
+                                                64 * c, td.row0);
+                            }
+                        } else {
+                            tc::mbar_arrive(&ms->kv_full[s]);
+                        }
+                    }
+                    continue;
+                }
+                // gathered tile: this thread's 32 slots
+                const __nv_bfloat16 *src[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int k = sgrp + 4 * m;
+                    const int32_t e = td.key0 + k;
+                    const __nv_bfloat16 *p = nullptr;
+                    if (k < td.n_valid) {
+                        if (e < ti.n_win) {
+                            p = a.ori_kv + (int64_t)(ti.win_start + e) * 512;
+                        } else {
+                            const int32_t ce = e - ti.n_win;
+                            p = a.cmp_kv + (int64_t)(a.cmp_idx ? list[ce] : ti.cmp_first + ce) * 512;
+                        }
+                    }
+                    src[m] = p;
+                }
                 for (int s = 0; s < 4; ++s) {
-                    ok = cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 12);
-                    if (!__all_sync(0xffffffffu, ok)) {
-                        broke = true;
+                    if (!cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 42)) {
+                        stop = true;
                         break;
                     }
-                    if (lane == 0) tc::mbar_expect_tx(&ms->kv_full[s], (uint32_t)n_groups * 1024u);
-                    __syncwarp();
-                    if (group_on) {
+                    const int c16 = 16 * s + col;             // 16-byte column in the row
+                    const int chunk = c16 >> 3, w = c16 & 7;  // 128-byte chunk, piece
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int c = 2 * s + cc;
-                            tc::tma_gather4(smem + kOffKV + c * 16384 + lane * 512, map,
-                                            &ms->kv_full[s], 64 * c, r[0], r[1], r[2], r[3]);
-                        }
+                    for (int m = 0; m < 32; ++m) {
+                        const int k = sgrp + 4 * m;
+                        if (src[m])
+                            cp_async16(kv_base + chunk * 16384 + k * 128 + ((w ^ (k & 7)) << 4),
+                                       src[m] + c16 * 8);
                     }
+                    cp_async_commit();
                 }
-                if (broke) break;
+                if (stop) break;
+                // All four slabs are in flight; release each as it lands (the
+                // tensor core cannot start this tile before the last one freed
+                // its slab anyway), visible to the async proxy.
+                cp_async_wait<3>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&ms->kv_full[0]);
+                cp_async_wait<2>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&ms->kv_full[1]);
+                cp_async_wait<1>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&ms->kv_full[2]);
+                cp_async_wait<0>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&ms->kv_full[3]);
             }
-            if (broke) break;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
         }
-        // ---- drain: every copy issued has landed before the CTA exits
-        if (lane == 0) {
-            if (q_n > 0 && !tc::mbar_wait(&ms->q_full, (q_n - 1) & 1)) cx.fail(13);
-            if (kv_n > 0)
-                for (int s = 0; s < 4; ++s)
-                    if (!tc::mbar_wait(&ms->kv_full[s], (kv_n - 1) & 1)) cx.fail(14);
-        }
-    } else if (warp == 1) {
+        cp_async_wait<0>();  // drain: no copy outlives the CTA
+        if (li == 0 && kv_n > 0)  // and no TMA copy either (last tile's phases)
+            for (int s = 0; s < 4; ++s)
+                if (!tc::mbar_wait(&ms->kv_full[s], (kv_n - 1) & 1)) cx.fail(43);
+    } else if (warp == 3) {
         // ========================================================= MMA warp
         if (lane == 0) {
             const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);
             const uint32_t id_o = tc::idesc_bf16(128, 64, true, true);
-            const uint32_t kv_a = tc::smem_u32(smem + kOffKV);
-            const uint32_t q_a = tc::smem_u32(smem + kOffQ);
-            const uint32_t p_a = tc::smem_u32(smem + kOffP);
+            // Descriptors of the four operand bases, built once; each MMA adds
+            // a constant byte offset (k-step, chunk, slab) to the address field.
+            const uint64_t ds_a = tc::smem_desc(tc::smem_u32(smem + kOffKV), 16, 1024);
+            const uint64_t ds_b = tc::smem_desc(tc::smem_u32(smem + kOffQ), 16, 1024);
+            const uint64_t do_a = tc::smem_desc(tc::smem_u32(smem + kOffKV), 16384, 1024);
+            const uint64_t do_b = tc::smem_desc(tc::smem_u32(smem + kOffP), 16384, 1024);
             uint32_t it = 0, q_n = 0, kv_n = 0, p_n = 0;
             bool issued = false;
             for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
@@ -357,12 +480,11 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 const TokenInfo ti = ms->info[slot];
                 tc::mbar_arrive(&ms->info_empty[slot]);
                 if (!ti.valid) continue;
-                if (!cx.wait(&ms->q_full, q_n & 1, 21)) break;
-                ++q_n;
                 bool stop = false;
                 for (int32_t j = 0; j < ti.n_tiles && !stop; ++j, ++kv_n) {
                     for (int s = 0; s < 4; ++s) {
-                        if (!cx.wait(&ms->kv_full[s], kv_n & 1, 22)) {
+                        if ((j == 0 && !cx.wait(&ms->q_full[s], q_n & 1, 21)) ||
+                            !cx.wait(&ms->kv_full[s], kv_n & 1, 22)) {
                             stop = true;
                             break;
                         }
@@ -372,15 +494,15 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             const int c = 2 * s + cc;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_bf16(tmem + kColS,
-                                             tc::smem_desc(kv_a + c * 16384 + kk * 32, 16, 1024),
-                                             tc::smem_desc(q_a + c * 8192 + kk * 32, 16, 1024),
-                                             id_s, (c | kk) != 0);
+                                tc::mma_bf16(tmem + kColS, tc::desc_add(ds_a, c * 16384 + kk * 32),
+                                             tc::desc_add(ds_b, c * 8192 + kk * 32), id_s,
+                                             (c | kk) != 0);
                         }
                         issued = true;
+                        // the last tile's S^T frees this pair of Q chunks
+                        if (j == ti.n_tiles - 1) tc::mma_commit(&ms->q_empty[s]);
                     }
                     if (stop) break;
-                    if (j == ti.n_tiles - 1) tc::mma_commit(&ms->q_empty);
                     tc::mma_commit(&ms->s_full);
                     if (!cx.wait(&ms->p_full, p_n & 1, 23)) {
                         stop = true;
@@ -392,13 +514,13 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             tc::mma_bf16(tmem + kColO + 64 * s,
-                                         tc::smem_desc(kv_a + 2 * s * 16384 + kk * 2048, 16384, 1024),
-                                         tc::smem_desc(p_a + kk * 2048, 16384, 1024), id_o,
-                                         (j > 0 || kk > 0));
+                                         tc::desc_add(do_a, 2 * s * 16384 + kk * 2048),
+                                         tc::desc_add(do_b, kk * 2048), id_o, (j > 0 || kk > 0));
                         tc::mma_commit(&ms->kv_empty[s]);
                     }
                 }
                 if (stop) break;
+                ++q_n;
                 tc::mma_commit(&ms->o_full);
             }
             if (issued) {
@@ -410,9 +532,14 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         __syncwarp();
     } else {
         // ================================================ softmax + epilogue
-        const int q4 = warp & 3;          // TMEM lane quarter of this warp
-        const int row = 32 * q4 + lane;   // key slot (softmax) / d row (epilogue)
-        const int ltid = tid - 64;        // 0..127
+        // Two warpgroups: wg 0 owns heads 0-31, wg 1 heads 32-63. Warp
+        // (4 + 4 wg + q) reads TMEM lane quarter q: one key slot per thread in
+        // the softmax, one d row of O^T per thread in the epilogue.
+        const int wg = (warp - 4) >> 2;
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;
+        const uint32_t bar_id = 1 + wg;
+        const int h0 = 32 * wg;                 // first head of this warpgroup
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         unsigned char *pbuf = smem + kOffP;
         const float c = a.softmax_scale * kLog2e;
@@ -420,151 +547,154 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
-            if (!bar_red_and(ok)) break;
+            if (!bar_red_and(bar_id, ok)) break;
             const TokenInfo ti = ms->info[slot];
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
             if (!ti.valid) continue;
-            if (ltid < 64) {
-                const float sink = (a.sinks && ltid < a.H) ? __ldg(a.sinks + ltid) : -INFINITY;
-                ms->m_run[ltid] = sink * kLog2e;
-            }
-            float lp[64];
+            // Per-head scalars live one head per lane (head h0 + lane):
+            // m_lane the running max (base 2); m_cur[] is every thread's copy
+            // of all 32, refreshed by shuffles only when some max moves.
+            float m_lane = ms->sink2[h0 + lane];
+            float lp[32], m_cur[32];
 #pragma unroll
-            for (int h = 0; h < 64; ++h) lp[h] = 0.0f;
+            for (int i = 0; i < 32; ++i) lp[i] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
             bool stop = false;
             for (int32_t j = 0; j < ti.n_tiles; ++j, ++tile_ctr) {
                 ok = cx.wait(&ms->s_full, s_n & 1, 31);
-                if (!bar_red_and(ok)) {
+                if (!bar_red_and(bar_id, ok)) {
                     stop = true;
                     break;
                 }
                 ++s_n;
                 tc::tc_fence_after();
-                float v[64];
-                {
-                    float x[32];
-                    tc::tmem_ld32(lane_addr + kColS, x);
-                    tc::tmem_wait_ld();
+                float v[32];
+                tc::tmem_ld32(lane_addr + kColS + h0, v);
+                tc::tmem_wait_ld();
+                const bool key_ok = row < tile_desc(ti, j).n_valid;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = x[i];
-                    tc::tmem_ld32(lane_addr + kColS + 32, x);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[32 + i] = x[i];
-                }
-                const int32_t sg = j * kTileKeys + row;
-                const bool key_ok = sg < ti.n_win || (sg >= ti.n_win4 && sg < ti.n_keys);
-#pragma unroll
-                for (int h = 0; h < 64; ++h) v[h] = key_ok ? v[h] * c : -INFINITY;
-                // tile max per head -> lazily moved running max
-                float m0, m1;
-                reduce_scatter64<true>(v, m0, m1, lane);
-                ms->red[q4][2 * lane] = m0;
-                ms->red[q4][2 * lane + 1] = m1;
+                for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
+                // tile max per head: warp maxima (one head per lane) across the
+                // four lane quarters; every warp derives the same lazy update
                 const uint32_t rs = tile_ctr & 1;
-                if (ltid == 0) ms->rescale[rs ^ 1] = 0;
-                tc::named_bar_sync(1, 128);
-                if (ltid < 64) {
-                    const float mt = fmaxf(fmaxf(ms->red[0][ltid], ms->red[1][ltid]),
-                                           fmaxf(ms->red[2][ltid], ms->red[3][ltid]));
-                    const float mo = ms->m_run[ltid];
-                    float al = 1.0f;
-                    if (mt > mo + kLazyMax) {
-                        al = (mo == -INFINITY) ? 0.0f : exp2f(mo - mt);
-                        ms->m_run[ltid] = mt;
-                        ms->rescale[rs] = 1;
-                    }
-                    ms->alpha[ltid] = al;
-                }
-                tc::named_bar_sync(1, 128);
-                if (ms->rescale[rs]) {
+                ms->red[rs][q4][h0 + lane] = reduce_scatter32<true>(v, lane);
+                tc::named_bar_sync(bar_id, 128);
+                const float mt = fmaxf(fmaxf(ms->red[rs][0][h0 + lane], ms->red[rs][1][h0 + lane]),
+                                       fmaxf(ms->red[rs][2][h0 + lane], ms->red[rs][3][h0 + lane]));
+                const bool up = mt > m_lane + kLazyMax;
+                const float al_lane = up ? (m_lane == -INFINITY ? 0.0f : tc::ex2_approx(m_lane - mt))
+                                         : 1.0f;
+                if (up) m_lane = mt;
+                if (__any_sync(0xffffffffu, up)) {  // uniform across the warpgroup
 #pragma unroll
-                    for (int h = 0; h < 64; ++h) lp[h] *= ms->alpha[h];
+                    for (int i = 0; i < 32; ++i) {
+                        m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
+                        lp[i] *= __shfl_sync(0xffffffffu, al_lane, i);
+                    }
                     if (j > 0) {
                         // O^T of the earlier tiles is complete (the commit that
-                        // signalled this S^T covers it); scale its columns.
+                        // signalled this S^T covers it); scale this half's columns.
 #pragma unroll 1
-                        for (int s = 0; s < 4; ++s) {
-#pragma unroll 1
-                            for (int half = 0; half < 2; ++half) {
-                                float x[32];
-                                const uint32_t addr = lane_addr + kColO + 64 * s + 32 * half;
-                                tc::tmem_ld32(addr, x);
-                                tc::tmem_wait_ld();
+                        for (int sl = 0; sl < 4; ++sl) {
+                            float x[32];
+                            const uint32_t addr = lane_addr + kColO + 64 * sl + h0;
+                            tc::tmem_ld32(addr, x);
+                            tc::tmem_wait_ld();
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) x[i] *= ms->alpha[32 * half + i];
-                                tc::tmem_st32(addr, x);
-                            }
+                            for (int i = 0; i < 32; ++i) x[i] *= __shfl_sync(0xffffffffu, al_lane, i);
+                            tc::tmem_st32(addr, x);
                         }
                         tc::tmem_wait_st();
                     }
                 }
-                // probabilities; P^T row `row` (64 heads = 128 B, MN-major SW128)
-                uint4 packed[8];
+                // Probabilities -> P^T row `row`, heads h0..h0+31 (64 B of the
+                // 128-byte MN-major SW128 row: 16-byte chunks 4 wg .. 4 wg + 3).
+                // m_cur is finite here: every tile holds a valid key, so the
+                // first tile always lifts an absent (-inf) sink.
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int cq = 0; cq < 4; ++cq) {
                     uint32_t w4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int h = 8 * ch + 2 * e;
-                        const float mu0 = ms->m_run[h], mu1 = ms->m_run[h + 1];
-                        const float p0 = (mu0 == -INFINITY) ? 0.0f : exp2f(v[h] - mu0);
-                        const float p1 = (mu1 == -INFINITY) ? 0.0f : exp2f(v[h + 1] - mu1);
-                        lp[h] += p0;
-                        lp[h + 1] += p1;
+                        const int i = 8 * cq + 2 * e;
+                        const float p0 = tc::ex2_approx(v[i] - m_cur[i]);
+                        const float p1 = tc::ex2_approx(v[i + 1] - m_cur[i + 1]);
+                        lp[i] += p0;
+                        lp[i + 1] += p1;
                         __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                         w4[e] = *reinterpret_cast<uint32_t *>(&pb);
                     }
-                    packed[ch] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
+                    const int ch = 4 * wg + cq;
                     *reinterpret_cast<uint4 *>(pbuf + row * 128 + ((ch ^ (row & 7)) * 16)) =
-                        packed[ch];
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_before();
                 tc::mbar_arrive(&ms->p_full);
             }
             if (stop) break;
-            // ---- epilogue: row sums, LSE, then O^T / l -> out[t, h, d]
-            {
-                float s0, s1;
-                reduce_scatter64<false>(lp, s0, s1, lane);
-                ms->red[q4][2 * lane] = s0;
-                ms->red[q4][2 * lane + 1] = s1;
-                tc::named_bar_sync(1, 128);
-                if (ltid < 64) {
-                    float l = (ms->red[0][ltid] + ms->red[1][ltid]) +
-                              (ms->red[2][ltid] + ms->red[3][ltid]);
-                    const float mu = ms->m_run[ltid];
-                    if (a.sinks && ltid < a.H) {
-                        const float sk = __ldg(a.sinks + ltid) * kLog2e;
-                        if (sk != -INFINITY) l += exp2f(sk - mu);
-                    }
-                    ms->inv_l[ltid] = l > 0.0f ? 1.0f / l : 0.0f;
-                    if (a.lse && ltid < a.H) a.lse[(int64_t)t * a.H + ltid] = (mu + log2f(l)) * kLn2;
-                }
-                tc::named_bar_sync(1, 128);
-            }
+            // ---- epilogue: row sums and LSE (one head per lane), then O^T / l
+            const uint32_t rs = tile_ctr & 1;  // a parity no softmax step of this token still reads
+            ms->red[rs][q4][h0 + lane] = reduce_scatter32<false>(lp, lane);
+            tc::named_bar_sync(bar_id, 128);
+            float l_lane = (ms->red[rs][0][h0 + lane] + ms->red[rs][1][h0 + lane]) +
+                           (ms->red[rs][2][h0 + lane] + ms->red[rs][3][h0 + lane]);
+            const float sk = ms->sink2[h0 + lane];
+            if (sk != -INFINITY) l_lane += tc::ex2_approx(sk - m_lane);
+            const float il_lane = l_lane > 0.0f ? tc::rcp_approx(l_lane) : 0.0f;
+            if (q4 == 0 && a.lse && h0 + lane < a.H)
+                a.lse[(int64_t)t * a.H + h0 + lane] = (m_lane + tc::lg2_approx(l_lane)) * kLn2;
+            float il[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) il[i] = __shfl_sync(0xffffffffu, il_lane, i);
             ok = cx.wait(&ms->o_full, o_n & 1, 32);
-            if (!bar_red_and(ok)) break;
+            if (!bar_red_and(bar_id, ok)) break;
             ++o_n;
             tc::tc_fence_after();
+            // O^T slab sl: this thread holds d = 128 sl + row for the 32 heads
+            // of its half. Lanes 8u..8u+7 transpose each 8 x 8 (d x head)
+            // block, so lane 8u+g ends with 8 consecutive d of head 8c+g: one
+            // 16-byte store per block; a warp writes 8 heads x 64 B at once.
             __nv_bfloat16 *outp = a.out + (int64_t)t * a.H * 512;
+            const int g = lane & 7;
 #pragma unroll 1
-            for (int s = 0; s < 4; ++s) {
-                const int d = 128 * s + row;
+            for (int sl = 0; sl < 4; ++sl) {
+                float x[32];
+                tc::tmem_ld32(lane_addr + kColO + 64 * sl + h0, x);
+                tc::tmem_wait_ld();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float x[32];
-                    tc::tmem_ld32(lane_addr + kColO + 64 * s + 32 * half, x);
-                    tc::tmem_wait_ld();
+                for (int i = 0; i < 32; ++i) x[i] *= il[i];
+                const int d0 = 128 * sl + 32 * q4 + 8 * (lane >> 3);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int h = 32 * half + i;
-                        if (h < a.H)
-                            outp[(int64_t)h * 512 + d] = __float2bfloat16_rn(x[i] * ms->inv_l[h]);
+                for (int cb = 0; cb < 4; ++cb) {
+                    float y[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) y[k] = x[8 * cb + k];
+#pragma unroll
+                    for (int m = 4; m >= 1; m >>= 1) {
+                        const bool hi = g & m;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (k & m) continue;  // pair (k, k ^ m), k the lower
+                            const float send = hi ? y[k] : y[k | m];
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+                            if (hi) y[k] = recv;
+                            else y[k | m] = recv;
+                        }
+                    }
+                    const int h = h0 + 8 * cb + g;
+                    if (h < a.H) {
+                        __nv_bfloat162 b0 = __floats2bfloat162_rn(y[0], y[1]);
+                        __nv_bfloat162 b1 = __floats2bfloat162_rn(y[2], y[3]);
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(y[4], y[5]);
+                        __nv_bfloat162 b3 = __floats2bfloat162_rn(y[6], y[7]);
+                        *reinterpret_cast<uint4 *>(outp + (int64_t)h * 512 + d0) =
+                            make_uint4(*reinterpret_cast<uint32_t *>(&b0),
+                                       *reinterpret_cast<uint32_t *>(&b1),
+                                       *reinterpret_cast<uint32_t *>(&b2),
+                                       *reinterpret_cast<uint32_t *>(&b3));
                     }
                 }
             }
@@ -575,7 +705,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+    if (warp == 3) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -590,18 +720,18 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     CUtensorMap q_map, ori_map, cmp_map;
     if (!encode_bf16_3d(&q_map, a.q, 512, a.H, a.T, 64, a.H, 1)) return cudaErrorInvalidValue;
-    if (!encode_bf16_2d(&ori_map, a.ori_kv, a.T, 512, 64, 1)) return cudaErrorInvalidValue;
+    if (!encode_bf16_2d(&ori_map, a.ori_kv, a.T, 512, 64, kTileKeys)) return cudaErrorInvalidValue;
     if (a.cmp_kv && a.Tc > 0) {
-        if (!encode_bf16_2d(&cmp_map, a.cmp_kv, a.Tc, 512, 64, 1)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&cmp_map, a.cmp_kv, a.Tc, 512, 64, kTileKeys))
+            return cudaErrorInvalidValue;
     } else {
-        cmp_map = ori_map;  // never read
+        cmp_map = ori_map;  // never read: no compressed tile exists
     }
     e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    Params p{a, a.window};
     const int ctas = a.T < sms ? a.T : sms;
-    sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, p);
+    sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, a);
     return cudaGetLastError();
 }
 

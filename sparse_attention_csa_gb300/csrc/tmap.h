@@ -37,9 +37,11 @@ inline bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D view [d2, d1, d0] (d0 contiguous), box {b0, b1, b2}.
+// 3-D view [d2, d1, d0] (d0 contiguous), box {b0, b1, b2}; 128-byte swizzle
+// unless `swizzle` is false (then the box is stored row-major in shared memory).
 inline bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
-                           uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
+                           uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2,
+                           bool swizzle = true) {
     auto fn = tensor_map_encoder();
     if (!fn || d2 == 0) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -47,7 +49,8 @@ inline bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -113,7 +113,7 @@ def test_mla_rejects(L):
     assert call(wl=1024) == 3
     assert call(r=1) == 3
     assert call(cuo=C.c_void_p(0x2000)) == 3  # prefix-KV cu_seqlens
-    assert call(topk=2049) == 3  # beyond the per-token index list
+    assert call(topk=1025) == 3  # beyond the per-token index list
     assert call(q=C.c_void_p(0x1002)) == 3  # 16-byte alignment
 
 
