@@ -59,7 +59,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=60)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="mixed32k", choices=list(packs.CONFIGS))
@@ -92,6 +92,15 @@ def max_over_ranks(x, world, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(step_ms, tokens_per_step, world, device):
+    """Whole-job throughput: every rank ran the same number of steps on its own
+    pack (replicas, weak scaling); time is the slowest rank's summed step time."""
+    total_ms = max_over_ranks(float(sum(step_ms)), world, device)
+    steps = len(step_ms)
+    return {"value": world * tokens_per_step * steps / (total_ms / 1e3),
+            "ms_per_step": total_ms / steps, "total_ms": total_ms}
 
 
 def load_peaks():
@@ -217,7 +226,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -383,9 +392,8 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {word:#x}")
 
-    total_ms = max_over_ranks(sum(step_ms), world, device)
-    value = world * T * args.steps / (total_ms / 1e3)
-    ms_per_step = total_ms / args.steps
+    agg = aggregate(step_ms, T, world, device)
+    value, ms_per_step = agg["value"], agg["ms_per_step"]
 
     # roofline of the dominant kernel
     peaks, peak_kind = load_peaks()
