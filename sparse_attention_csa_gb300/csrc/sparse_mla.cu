@@ -32,15 +32,21 @@
 //     every visible block) and at least half a tile long, else gathered by
 //     cp.async. Rows of a box past the tile's valid count are masked. (TMA
 //     gather4 moves single 128-byte rows an order of magnitude slower than
-//     these paths.) Q arrives by 3-D TMA.
-//   * Warp roles: 0 scheduler (key lists, Q), 1-2 loaders (K/V tiles),
+//     these paths.) Q arrives by 3-D TMA, after an L2 prefetch issued one token ahead.
+//   * Warp roles: 0 scheduler (key lists, Q), 1-2 loaders (K/V tiles;
+//     gathered slabs are released by cp.async-tracking mbarrier arrivals),
 //     3 tensor memory + tcgen05.mma issue (one thread), 4-11 softmax and
 //     epilogue in two warpgroups of 32 heads each (softmax: one thread per key
 //     = one TMEM lane, 32 head scores; epilogue: one thread per d row of O^T,
-//     8 x 8 blocks transposed across lanes in registers, 16-byte stores).
+//     so a warp's lanes hold 32 consecutive d of each head: 64-byte stores
+//     with no data exchanged between lanes. Lane shuffles and cp.async traffic
+//     both slow the tensor core's concurrent shared-memory reads, so the
+//     kernel keeps them off the common path).
 //   * Online softmax in base 2 with a lazily moved running max: a head's max
 //     only moves when a tile exceeds it by more than 8 (a factor 256), so O^T
-//     in tensor memory is rescaled rarely. Row sums accumulate per thread in
+//     in tensor memory is rescaled rarely, and the cross-lane reduction of the
+//     tile maxima runs only for tiles where some score exceeds a max by that
+//     much (a warpgroup-wide vote decides). Row sums accumulate per thread in
 //     fp32 and are reduced once per token.
 //   * Every mbarrier wait is bounded; a timeout records CSA_ERR_TIMEOUT, the
 //     CTA drains its copies and MMAs, frees tensor memory and exits.
@@ -61,6 +67,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.0f;  // base-2 units
 constexpr int kMinBoxRows = 64;   // shorter compressed runs are gathered, not boxed
+#ifndef CSA_MLA_CHUNK
+#define CSA_MLA_CHUNK 1
+#endif
+constexpr int kChunk = CSA_MLA_CHUNK;  // consecutive tokens per CTA visit
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffKV = 0;            // 8 chunks x [128 keys x 128 B]
@@ -102,6 +112,14 @@ __device__ __forceinline__ TileDesc tile_desc(const TokenInfo &ti, int32_t j) {
     return {kTileGather, 0, n, ti.n_win + jc * kTileKeys};
 }
 
+// The it-th token of this CTA: runs of kChunk consecutive tokens, run r of
+// the grid going to CTA r mod gridDim.x. Increasing in `it`.
+__device__ __forceinline__ int32_t token_at(uint32_t it) {
+    const int64_t run = (int64_t)(it / kChunk) * gridDim.x + blockIdx.x;
+    const int64_t t = run * kChunk + it % kChunk;
+    return t < INT32_MAX ? (int32_t)t : INT32_MAX;
+}
+
 struct Misc {
     uint64_t q_full[4], q_empty[4];   // per pair of 64-wide chunks of Q
     uint64_t kv_full[4], kv_empty[4]; // per slab (pair of chunks) of the K/V tile
@@ -134,12 +152,28 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, bool v) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
+// The mbarrier counts one arrival (already included in its expected count)
+// once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar))
+                 : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// OR of v over the 128 threads of named barrier `id`.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return out != 0;
 }
 
 struct Ctx {
@@ -258,7 +292,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // ================================================== scheduler warp
         uint32_t it = 0, q_n = 0;
         int32_t seg_lo = 0, seg_hi = 0, seg_b = -1;  // last sequence found: [lo, hi)
-        for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
+        for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
             const uint32_t slot = it & 1;
             // the slot's key list is rewritten only once every consumer is done
             bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
@@ -340,6 +374,10 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             if (lane == 0) {
                 ms->info[slot] = ti;
                 tc::mbar_arrive(&ms->info_full[slot]);
+                // Q of this CTA's next token streams from HBM into L2 while
+                // this token runs; its TMA load then hits L2.
+                const int32_t tn = token_at(it + 1);
+                if (tn < a.T) tc::prefetch_l2_bulk(a.q + (int64_t)tn * a.H * 512, (uint32_t)a.H * 1024u);
             }
             if (!ti.valid) continue;
             // Q rows of token t (H rows of 512; rows >= H stay zero), one pair
@@ -377,7 +415,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         uint32_t it = 0, kv_n = 0;
         const uint32_t kv_base = tc::smem_u32(smem + kOffKV);
         bool stop = false;
-        for (int32_t t = blockIdx.x; t < a.T && !stop; t += gridDim.x, ++it) {
+        for (int32_t t = token_at(it); t < a.T && !stop; t = token_at(++it)) {
             const uint32_t slot = it & 1;
             if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40)) break;
             const TokenInfo ti = ms->info[slot];
@@ -421,6 +459,9 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                     src[m] = p;
                 }
+                // Each slab is released to the tensor core by the mbarrier
+                // itself once this thread's copies land; the thread goes on to
+                // the next slab without waiting.
                 for (int s = 0; s < 4; ++s) {
                     if (!cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 42)) {
                         stop = true;
@@ -435,29 +476,13 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             cp_async16(kv_base + chunk * 16384 + k * 128 + ((w ^ (k & 7)) << 4),
                                        src[m] + c16 * 8);
                     }
-                    cp_async_commit();
+                    cp_async_arrive(&ms->kv_full[s]);
                 }
-                if (stop) break;
-                // All four slabs are in flight; release each as it lands (the
-                // tensor core cannot start this tile before the last one freed
-                // its slab anyway), visible to the async proxy.
-                cp_async_wait<3>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&ms->kv_full[0]);
-                cp_async_wait<2>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&ms->kv_full[1]);
-                cp_async_wait<1>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&ms->kv_full[2]);
-                cp_async_wait<0>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&ms->kv_full[3]);
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
         }
-        cp_async_wait<0>();  // drain: no copy outlives the CTA
+        cp_async_wait_all();  // drain: no copy outlives the CTA
         if (li == 0 && kv_n > 0)  // and no TMA copy either (last tile's phases)
             for (int s = 0; s < 4; ++s)
                 if (!tc::mbar_wait(&ms->kv_full[s], (kv_n - 1) & 1)) cx.fail(43);
@@ -474,7 +499,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const uint64_t do_b = tc::smem_desc(tc::smem_u32(smem + kOffP), 16384, 1024);
             uint32_t it = 0, q_n = 0, kv_n = 0, p_n = 0;
             bool issued = false;
-            for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
+            for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
                 const uint32_t slot = it & 1;
                 if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
                 const TokenInfo ti = ms->info[slot];
@@ -488,6 +513,9 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             stop = true;
                             break;
                         }
+                        // slabs gathered by cp.async were written through the
+                        // generic proxy: order them before the tensor core's reads
+                        tc::fence_proxy_async_smem();
                         tc::tc_fence_after();
 #pragma unroll
                         for (int cc = 0; cc < 2; ++cc) {
@@ -544,7 +572,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         unsigned char *pbuf = smem + kOffP;
         const float c = a.softmax_scale * kLog2e;
         uint32_t it = 0, s_n = 0, o_n = 0, tile_ctr = 0;
-        for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
+        for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
             if (!bar_red_and(bar_id, ok)) break;
@@ -576,37 +604,47 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 const bool key_ok = row < tile_desc(ti, j).n_valid;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
-                // tile max per head: warp maxima (one head per lane) across the
-                // four lane quarters; every warp derives the same lazy update
-                const uint32_t rs = tile_ctr & 1;
-                ms->red[rs][q4][h0 + lane] = reduce_scatter32<true>(v, lane);
-                tc::named_bar_sync(bar_id, 128);
-                const float mt = fmaxf(fmaxf(ms->red[rs][0][h0 + lane], ms->red[rs][1][h0 + lane]),
-                                       fmaxf(ms->red[rs][2][h0 + lane], ms->red[rs][3][h0 + lane]));
-                const bool up = mt > m_lane + kLazyMax;
-                const float al_lane = up ? (m_lane == -INFINITY ? 0.0f : tc::ex2_approx(m_lane - mt))
-                                         : 1.0f;
-                if (up) m_lane = mt;
-                if (__any_sync(0xffffffffu, up)) {  // uniform across the warpgroup
+                // A head's max moves only when some score of this tile exceeds
+                // it by more than kLazyMax; the warpgroup first checks whether
+                // any does, and only then reduces the tile maxima.
+                bool exceeds = false;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
-                        lp[i] *= __shfl_sync(0xffffffffu, al_lane, i);
-                    }
-                    if (j > 0) {
-                        // O^T of the earlier tiles is complete (the commit that
-                        // signalled this S^T covers it); scale this half's columns.
-#pragma unroll 1
-                        for (int sl = 0; sl < 4; ++sl) {
-                            float x[32];
-                            const uint32_t addr = lane_addr + kColO + 64 * sl + h0;
-                            tc::tmem_ld32(addr, x);
-                            tc::tmem_wait_ld();
+                for (int i = 0; i < 32; ++i) exceeds |= v[i] > m_cur[i] + kLazyMax;
+                if (bar_red_or(bar_id, exceeds)) {
+                    // tile max per head: warp maxima (one head per lane) across the
+                    // four lane quarters; every warp derives the same lazy update
+                    const uint32_t rs = tile_ctr & 1;
+                    ms->red[rs][q4][h0 + lane] = reduce_scatter32<true>(v, lane);
+                    tc::named_bar_sync(bar_id, 128);
+                    const float mt =
+                        fmaxf(fmaxf(ms->red[rs][0][h0 + lane], ms->red[rs][1][h0 + lane]),
+                              fmaxf(ms->red[rs][2][h0 + lane], ms->red[rs][3][h0 + lane]));
+                    const bool up = mt > m_lane + kLazyMax;
+                    const float al_lane =
+                        up ? (m_lane == -INFINITY ? 0.0f : tc::ex2_approx(m_lane - mt)) : 1.0f;
+                    if (up) m_lane = mt;
+                    if (__any_sync(0xffffffffu, up)) {  // uniform across the warpgroup
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) x[i] *= __shfl_sync(0xffffffffu, al_lane, i);
-                            tc::tmem_st32(addr, x);
+                        for (int i = 0; i < 32; ++i) {
+                            m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
+                            lp[i] *= __shfl_sync(0xffffffffu, al_lane, i);
                         }
-                        tc::tmem_wait_st();
+                        if (j > 0) {
+                            // O^T of the earlier tiles is complete (the commit that
+                            // signalled this S^T covers it); scale this half's columns.
+#pragma unroll 1
+                            for (int sl = 0; sl < 4; ++sl) {
+                                float x[32];
+                                const uint32_t addr = lane_addr + kColO + 64 * sl + h0;
+                                tc::tmem_ld32(addr, x);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    x[i] *= __shfl_sync(0xffffffffu, al_lane, i);
+                                tc::tmem_st32(addr, x);
+                            }
+                            tc::tmem_wait_st();
+                        }
                     }
                 }
                 // Probabilities -> P^T row `row`, heads h0..h0+31 (64 B of the
@@ -654,49 +692,19 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             ++o_n;
             tc::tc_fence_after();
             // O^T slab sl: this thread holds d = 128 sl + row for the 32 heads
-            // of its half. Lanes 8u..8u+7 transpose each 8 x 8 (d x head)
-            // block, so lane 8u+g ends with 8 consecutive d of head 8c+g: one
-            // 16-byte store per block; a warp writes 8 heads x 64 B at once.
-            __nv_bfloat16 *outp = a.out + (int64_t)t * a.H * 512;
-            const int g = lane & 7;
+            // of its half, and the warp's 32 lanes hold 32 consecutive d: for
+            // each head the warp writes one contiguous 64-byte piece of the
+            // head's output row. No data moves between lanes.
+            const int n_h = min(32, a.H - h0);  // heads of this half that exist
+            __nv_bfloat16 *outp = a.out + (int64_t)t * a.H * 512 + (int64_t)h0 * 512 + row;
 #pragma unroll 1
-            for (int sl = 0; sl < 4; ++sl) {
+            for (int sl = 0; sl < 4 && n_h > 0; ++sl) {
                 float x[32];
                 tc::tmem_ld32(lane_addr + kColO + 64 * sl + h0, x);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] *= il[i];
-                const int d0 = 128 * sl + 32 * q4 + 8 * (lane >> 3);
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    float y[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) y[k] = x[8 * cb + k];
-#pragma unroll
-                    for (int m = 4; m >= 1; m >>= 1) {
-                        const bool hi = g & m;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            if (k & m) continue;  // pair (k, k ^ m), k the lower
-                            const float send = hi ? y[k] : y[k | m];
-                            const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-                            if (hi) y[k] = recv;
-                            else y[k | m] = recv;
-                        }
-                    }
-                    const int h = h0 + 8 * cb + g;
-                    if (h < a.H) {
-                        __nv_bfloat162 b0 = __floats2bfloat162_rn(y[0], y[1]);
-                        __nv_bfloat162 b1 = __floats2bfloat162_rn(y[2], y[3]);
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(y[4], y[5]);
-                        __nv_bfloat162 b3 = __floats2bfloat162_rn(y[6], y[7]);
-                        *reinterpret_cast<uint4 *>(outp + (int64_t)h * 512 + d0) =
-                            make_uint4(*reinterpret_cast<uint32_t *>(&b0),
-                                       *reinterpret_cast<uint32_t *>(&b1),
-                                       *reinterpret_cast<uint32_t *>(&b2),
-                                       *reinterpret_cast<uint32_t *>(&b3));
-                    }
-                }
+                for (int i = 0; i < 32; ++i)
+                    if (i < n_h) outp[(int64_t)i * 512 + 128 * sl] = __float2bfloat16_rn(x[i] * il[i]);
             }
             tc::tc_fence_before();
         }
@@ -730,7 +738,8 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int ctas = a.T < sms ? a.T : sms;
+    const int64_t runs = ((int64_t)a.T + kChunk - 1) / kChunk;
+    const int ctas = runs < sms ? (int)runs : sms;
     sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, a);
     return cudaGetLastError();
 }
