@@ -14,7 +14,7 @@
 //     l_i = scale * q.kv_i ; m = max(l, sink) ; Z = sum e^(l_i-m) + e^(sink-m)
 //     out = sum e^(l_i-m) kv_i / Z ; lse = m + ln Z
 //
-// Design (one token per CTA iteration, persistent grid, 1 CTA per SM):
+// Design (persistent grid, 1 CTA per SM, one token at a time per CTA):
 //   * All H (<= 64, padded to 64) heads of a token share its key rows, so the
 //     contraction is done transposed, with the keys on the MMA's M side:
 //         S^T[key, h]  = K[key, :] . Q[h, :]        M=128 keys, N=64, K=512
@@ -23,25 +23,29 @@
 //     (SW128, K-major) serves S^T as the A operand and, read MN-major, O^T as
 //     the A operand. Accumulators live in tensor memory: S^T in 64 columns,
 //     O^T in 4 x 64 columns.
-//   * Key tiles. A token with at most 128 keys gets one tile: its window rows
-//     then its compressed rows, gathered with 16-byte cp.async. Otherwise its
-//     window rows (one contiguous run) fill tiles of their own, loaded by 2-D
-//     TMA boxes of 128 rows, and its compressed rows follow in their own
-//     tiles: by TMA boxes too when they form one ascending run (always in the
-//     compressor-only mode, and in the indexer mode whenever top-k covers
-//     every visible block) and at least half a tile long, else gathered by
-//     cp.async. Rows of a box past the tile's valid count are masked. (TMA
-//     gather4 moves single 128-byte rows an order of magnitude slower than
-//     these paths.) Q arrives by 3-D TMA, after an L2 prefetch issued one token ahead.
-//   * Warp roles: 0 scheduler (key lists, Q), 1-2 loaders (K/V tiles;
-//     gathered slabs are released by cp.async-tracking mbarrier arrivals),
-//     3 tensor memory + tcgen05.mma issue (one thread), 4-11 softmax and
-//     epilogue in two warpgroups of 32 heads each (softmax: one thread per key
-//     = one TMEM lane, 32 head scores; epilogue: one thread per d row of O^T,
-//     so a warp's lanes hold 32 consecutive d of each head: 64-byte stores
-//     with no data exchanged between lanes. Lane shuffles and cp.async traffic
-//     both slow the tensor core's concurrent shared-memory reads, so the
-//     kernel keeps them off the common path).
+//   * Work split. Each CTA takes one contiguous range of tokens, balanced by a
+//     closed-form model of the tiles per token, so that consecutive tokens of
+//     a sequence follow each other in one CTA.
+//   * Key tiles (kinds below) have slot layouts fixed by the token alone, and
+//     a token at an even position runs its tiles in the natural order (window
+//     first), one at an odd position in reverse. The last tile of a token is
+//     then the first tile of the next one, which takes it over with at most
+//     its own row and a newly visible block loaded (cp.async): the window as
+//     a ring of 128 slots, compressed runs as 128-row boxes that already hold
+//     the later blocks. Whole tiles come by 2-D TMA boxes (window rings,
+//     contiguous compressed runs) or 16-byte cp.async gathers (top-k lists,
+//     short mixed key sets); rows of a box past the token's keys are masked.
+//     Results do not depend on the split: every layout and order is a
+//     function of the token. Q arrives by 3-D TMA after an L2 prefetch issued
+//     one token ahead.
+//   * Warp roles: 0 scheduler (key lists, tile plans, Q), 1-2 loaders (K/V
+//     tiles; gathered rows are released by cp.async-tracking mbarrier
+//     arrivals), 3 tensor memory + tcgen05.mma issue (one thread; it waits on
+//     one barrier per tile and issues the 32 S^T MMAs back to back), 4-11
+//     softmax and epilogue in two warpgroups of 32 heads each (softmax: one
+//     thread per key = one TMEM lane, 32 head scores; epilogue: one thread per
+//     d row of O^T, so a warp's lanes hold 32 consecutive d of each head:
+//     64-byte stores with no data exchanged between lanes).
 //   * Online softmax in base 2 with a lazily moved running max: a head's max
 //     only moves when a tile exceeds it by more than 8 (a factor 256), so O^T
 //     in tensor memory is rescaled rarely, and the cross-lane reduction of the
@@ -67,10 +71,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyMax = 8.0f;  // base-2 units
 constexpr int kMinBoxRows = 64;   // shorter compressed runs are gathered, not boxed
-#ifndef CSA_MLA_CHUNK
-#define CSA_MLA_CHUNK 1
-#endif
-constexpr int kChunk = CSA_MLA_CHUNK;  // consecutive tokens per CTA visit
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffKV = 0;            // 8 chunks x [128 keys x 128 B]
@@ -84,49 +84,226 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 
-enum : int32_t { kTileOri = 0, kTileCmp = 1, kTileGather = 2 };
-enum : int32_t { kFlagMixed = 1, kFlagCmpRun = 2 };
+// Tile kinds. Every kind has a fixed slot layout that depends only on the
+// token (never on which CTA runs it or what it ran before), so a tile left in
+// shared memory by one token can be taken over by the next token of the same
+// sequence with at most a row or two loaded, and results stay bit-identical
+// however the tokens are split between CTAs.
+//   kRing   window rows of ori_kv in a ring: row r in slot (r - b0) mod 128,
+//           b0 a base fixed by the token's position; optionally the first
+//           n_top compressed rows of the sequence in the top slots
+//           (compressed row j in slot 127 - j) when they fit beside the window.
+//           Loaded as one 128-row TMA box from b0 (rows past the token are
+//           future window rows, masked), or gathered when top rows are present.
+//   kWinBox window rows win_start + 128 j + slot (windows wider than 128).
+//   kCmpBox compressed rows c0 + slot of one ascending run (TMA box).
+//   kGather compressed entries e0 + slot of the token's index list (cp.async).
+//   kGMix   window rows then compressed entries, gathered (short key sets
+//           whose window already slides, or whose compressed set is a top-k).
+enum : int32_t { kRing = 0, kWinBox = 1, kCmpBox = 2, kGather = 3, kGMix = 4 };
+enum : int32_t { kFlagRun = 1, kFlagAllVis = 2 };
 
 struct TokenInfo {
-    int32_t t, n_win, n_cmp, n_tiles;
-    int32_t valid, win_start, cmp_first, flags;
+    int32_t t, valid, pos, seg;          // token, position in its sequence, sequence
+    int32_t win_start, n_win, cbase, n_cmp;  // window; first compressed row of the
+                                             // sequence; valid compressed keys
+    int32_t cmp_first, flags, b0, n_top;     // first compressed row (runs); ring base
+    int32_t n_wt, n_ct, n_tiles, single;     // window / compressed / all tiles; single-tile kind or -1
+    int32_t reuse, n_delta;                  // first tile taken over from the previous token
+    int32_t d_row[2], d_slot[2], d_cmp[2];   // rows loaded into it (d_cmp: from cmp_kv)
 };
 
 struct TileDesc {
-    int32_t kind;     // kTileOri / kTileCmp (TMA box of 128 rows from row0) or kTileGather
-    int32_t row0;     // first row of the box
-    int32_t n_valid;  // slots [0, n_valid) hold keys
-    int32_t key0;     // key index (window rows first, then compressed) of slot 0
+    int32_t kind;
+    int32_t row0;     // kRing: b0; kWinBox / kCmpBox: first row of the box
+    int32_t n_valid;  // kRing: n_top; others: slots [0, n_valid) hold keys
+    int32_t e0;       // kGather: first list entry
 };
 
-__device__ __forceinline__ TileDesc tile_desc(const TokenInfo &ti, int32_t j) {
-    if (ti.flags & kFlagMixed) return {kTileGather, 0, ti.n_win + ti.n_cmp, 0};
-    const int32_t nwt = (ti.n_win + kTileKeys - 1) / kTileKeys;
-    if (j < nwt)
-        return {kTileOri, ti.win_start + j * kTileKeys, min(kTileKeys, ti.n_win - j * kTileKeys),
-                j * kTileKeys};
-    const int32_t jc = j - nwt;
-    const int32_t n = min(kTileKeys, ti.n_cmp - jc * kTileKeys);
-    if ((ti.flags & kFlagCmpRun) && n >= kMinBoxRows)
-        return {kTileCmp, ti.cmp_first + jc * kTileKeys, n, ti.n_win + jc * kTileKeys};
-    return {kTileGather, 0, n, ti.n_win + jc * kTileKeys};
+// Natural tile order: window tile(s), then compressed tiles. Tokens at even
+// positions run it forwards and tokens at odd positions backwards, so the
+// last tile of one token is the first tile of the next one.
+__device__ __forceinline__ int32_t tile_nat(const TokenInfo &ti, int32_t j) {
+    return (ti.pos & 1) ? ti.n_tiles - 1 - j : j;
 }
 
-// The it-th token of this CTA: runs of kChunk consecutive tokens, run r of
-// the grid going to CTA r mod gridDim.x. Increasing in `it`.
-__device__ __forceinline__ int32_t token_at(uint32_t it) {
-    const int64_t run = (int64_t)(it / kChunk) * gridDim.x + blockIdx.x;
-    const int64_t t = run * kChunk + it % kChunk;
-    return t < INT32_MAX ? (int32_t)t : INT32_MAX;
+__device__ __forceinline__ TileDesc tile_at(const TokenInfo &ti, int32_t nat) {
+    if (ti.single == kRing) return {kRing, ti.b0, ti.n_top, 0};
+    if (ti.single == kGMix) return {kGMix, 0, ti.n_win + ti.n_cmp, 0};
+    if (nat < ti.n_wt) {
+        if (ti.n_wt == 1 && ti.b0 >= 0) return {kRing, ti.b0, 0, 0};
+        return {kWinBox, ti.win_start + nat * kTileKeys,
+                min(kTileKeys, ti.n_win - nat * kTileKeys), 0};
+    }
+    const int32_t k = nat - ti.n_wt;
+    const int32_t n = min(kTileKeys, ti.n_cmp - k * kTileKeys);
+    if ((ti.flags & kFlagRun) && ((ti.flags & kFlagAllVis) || n >= kMinBoxRows))
+        return {kCmpBox, ti.cmp_first + k * kTileKeys, n, 0};
+    return {kGather, 0, n, k * kTileKeys};
+}
+
+// A ring tile is loaded whole as one TMA box from its base when it has no
+// compressed rows on top and the token's own row falls inside the box (a
+// token at an even position whose window already slides needs one row past
+// it, so its ring is gathered instead).
+__device__ __forceinline__ bool ring_box(const TokenInfo &ti, const TileDesc &td) {
+    return td.kind == kRing && td.n_valid == 0 && ti.t <= td.row0 + kTileKeys - 1;
+}
+
+// Does slot `s` of tile `td` hold one of token ti's keys?
+__device__ __forceinline__ bool slot_valid(const TokenInfo &ti, const TileDesc &td, int32_t s) {
+    if (td.kind != kRing) return s < td.n_valid;
+    if (s >= kTileKeys - td.n_valid) return true;  // compressed rows on top
+    const int32_t r = ti.t - ((ti.t - td.row0 - s) & (kTileKeys - 1));
+    return r >= ti.win_start;
+}
+
+// ---------------------------------------------------------------- work split
+// Each CTA runs one contiguous range of tokens, so consecutive tokens of a
+// sequence meet in the same CTA. The ranges split a work model evenly: a token
+// costs kTokenCost plus kTileCost per key tile (the time goes mostly per tile).
+// With nw(p) = min(W, p+1) window keys and nc(p) = min(Kcap, floor((p+1)/r))
+// compressed keys at position p, a token has one tile when nw + nc <= 128,
+// else ceil(nw/128) + ceil(nc/128) (one ring tile when W <= 128). The prefix
+// sums over a sequence are closed forms over the few positions where a
+// ceiling steps. Compressed tiles gathered from a top-k list (positions that
+// see more blocks than top-k keeps) cost a little more than boxed runs.
+constexpr int64_t kTokenCost = 3;
+constexpr int64_t kTileCost = 8;
+constexpr int64_t kGatherCost = 3;  // extra for a compressed tile gathered from a top-k list
+
+struct WorkModel {
+    int64_t W, r, kcap;  // kcap < 0: no cap; r == 0: no compressed keys
+    int64_t p1;          // first position with more than one tile
+    __device__ __forceinline__ int64_t nc(int64_t p) const {
+        if (r <= 0) return 0;
+        const int64_t v = (p + 1) / r;
+        return kcap < 0 ? v : min(v, kcap);
+    }
+    __device__ __forceinline__ int64_t keys(int64_t p) const { return min(W, p + 1) + nc(p); }
+    __device__ void init(int64_t W_, int64_t r_, int64_t kcap_) {
+        W = W_;
+        r = r_;
+        kcap = kcap_;
+        // keys(p) grows with p and exceeds 128 by p = 128 at the latest
+        int64_t lo = 0, hi = kTileKeys;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (keys(mid) > kTileKeys) hi = mid;
+            else lo = mid + 1;
+        }
+        p1 = lo;
+    }
+    // #{p in [a, b) : nc(p) > 128 k}, summed over k >= 0
+    __device__ __forceinline__ int64_t cmp_tiles(int64_t a, int64_t b) const {
+        int64_t s = 0;
+        if (r <= 0) return 0;
+        for (int64_t k = 0;; ++k) {
+            if (kcap >= 0 && kcap <= kTileKeys * k) break;
+            const int64_t thr = r * (kTileKeys * k + 1) - 1;  // nc(p) > 128 k  <=>  p >= thr
+            if (thr >= b) break;
+            s += b - max(a, thr);
+        }
+        return s;
+    }
+    // #{p in [a, b) : nw(p) > 128 k}, summed over k >= 0
+    __device__ __forceinline__ int64_t win_tiles(int64_t a, int64_t b) const {
+        int64_t s = 0;
+        for (int64_t k = 0; W > kTileKeys * k && kTileKeys * k < b; ++k)
+            s += b - max(a, kTileKeys * k);
+        return s;
+    }
+    // cost of the first P positions of a sequence
+    __device__ int64_t prefix(int64_t P) const {
+        if (P <= 0) return 0;
+        int64_t tiles = min(P, p1), gathered = 0;
+        if (p1 < P) {
+            tiles += (W <= kTileKeys ? P - p1 : win_tiles(p1, P)) + cmp_tiles(p1, P);
+            if (r > 0 && kcap >= 0) {  // positions that see more blocks than top-k keeps
+                const int64_t pg = max(p1, r * (kcap + 1) - 1);
+                if (P > pg) gathered = (P - pg) * ((kcap + kTileKeys - 1) / kTileKeys);
+            }
+        }
+        return kTokenCost * P + kTileCost * tiles + kGatherCost * gathered;
+    }
+};
+
+// [*lo, *hi) for this CTA; run by one whole warp.
+__device__ void cta_token_range(const MlaArgs &a, bool use_cmp, int lane, int32_t *lo,
+                                int32_t *hi) {
+    WorkModel wm;
+    wm.init(a.window, use_cmp ? a.cmp_ratio : 0, a.cmp_idx ? a.topk : -1);
+    const int64_t G = gridDim.x, c = blockIdx.x;
+    // pass 1: total cost and a sanity check of cu_seqlens
+    int64_t total = 0;
+    bool sane = a.batch >= 0 && __ldg(a.cu_q) >= 0 && __ldg(a.cu_q + a.batch) <= a.T;
+    for (int32_t b0 = 0; b0 < a.batch; b0 += 32) {
+        const int32_t b = b0 + lane;
+        int64_t cost = 0;
+        if (b < a.batch) {
+            const int32_t L = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
+            sane &= L >= 0;
+            cost = wm.prefix(max(L, 0));
+        }
+        for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
+        total += cost;
+    }
+    sane = __all_sync(0xffffffffu, sane);
+    if (!sane || total <= 0) {  // fall back to an even split of the token range
+        if (!sane && lane == 0 && c == 0) report_error(a.err, kErrCheck, kKerMla, 3);
+        *lo = (int32_t)((int64_t)a.T * c / G);
+        *hi = (int32_t)((int64_t)a.T * (c + 1) / G);
+        return;
+    }
+    const int64_t S[2] = {total * c / G, total * (c + 1) / G};
+    int32_t res[2] = {a.T, a.T};
+    int64_t carry = 0;
+    for (int32_t b0 = 0; b0 < a.batch; b0 += 32) {
+        const int32_t b = b0 + lane;
+        int64_t cost = 0;
+        int32_t L = 0, start = 0;
+        if (b < a.batch) {
+            start = __ldg(a.cu_q + b);
+            L = __ldg(a.cu_q + b + 1) - start;
+            cost = wm.prefix(L);
+        }
+        int64_t incl = cost;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int64_t before = carry + incl - cost;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            // first token whose preceding cost reaches S[k]
+            const bool mine = cost > 0 && before <= S[k] && S[k] < before + cost;
+            int32_t t = a.T;
+            if (mine) {
+                int64_t lo_p = 0, hi_p = L;  // smallest P with before + prefix(P) >= S
+                while (lo_p < hi_p) {
+                    const int64_t mid = (lo_p + hi_p) >> 1;
+                    if (before + wm.prefix(mid) >= S[k]) hi_p = mid;
+                    else lo_p = mid + 1;
+                }
+                t = start + (int32_t)lo_p;
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, mine);
+            if (m) res[k] = __shfl_sync(0xffffffffu, t, __ffs(m) - 1);
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    *lo = c == 0 ? 0 : res[0];
+    *hi = c == G - 1 ? a.T : res[1];
 }
 
 struct Misc {
-    uint64_t q_full[4], q_empty[4];   // per pair of 64-wide chunks of Q
-    uint64_t kv_full[4], kv_empty[4]; // per slab (pair of chunks) of the K/V tile
+    uint64_t q_full, q_empty;         // Q of the token
+    uint64_t kv_full, kv_empty[4];    // K/V tile landed; released per slab (pair of chunks)
     uint64_t s_full, p_full, o_full, drain;
     uint64_t info_full[2], info_empty[2];
     uint32_t tmem_base;
     int32_t abort;
+    int32_t range_lo, range_hi;  // this CTA's tokens
     TokenInfo info[2];
     __align__(16) float red[2][4][64];   // [tile parity][lane quarter][head]
     __align__(16) float sink2[64];       // sink * log2(e), -inf when absent
@@ -250,12 +427,10 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        for (int s = 0; s < 4; ++s) {
-            tc::mbar_init(&ms->q_full[s], 1);
-            tc::mbar_init(&ms->q_empty[s], 1);
-            tc::mbar_init(&ms->kv_full[s], kLoaders);
-            tc::mbar_init(&ms->kv_empty[s], 1);
-        }
+        tc::mbar_init(&ms->q_full, 1);
+        tc::mbar_init(&ms->q_empty, 1);
+        tc::mbar_init(&ms->kv_full, kLoaders);
+        for (int s = 0; s < 4; ++s) tc::mbar_init(&ms->kv_empty[s], 1);
         tc::mbar_init(&ms->s_full, 1);
         tc::mbar_init(&ms->p_full, 256);
         tc::mbar_init(&ms->o_full, 1);
@@ -277,28 +452,44 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         tc::tmem_alloc(&ms->tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        tc::tma_prefetch_desc(&q_map);
-        tc::tma_prefetch_desc(&ori_map);
-        tc::tma_prefetch_desc(&cmp_map);
+    const bool use_cmp = a.cmp_kv != nullptr && a.Tc > 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&q_map);
+            tc::tma_prefetch_desc(&ori_map);
+            tc::tma_prefetch_desc(&cmp_map);
+        }
+        int32_t lo, hi;
+        cta_token_range(a, use_cmp, lane, &lo, &hi);
+        if (lane == 0) {
+            ms->range_lo = lo;
+            ms->range_hi = hi;
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const bool use_cmp = a.cmp_kv != nullptr && a.Tc > 0;
+    const int32_t t_lo = ms->range_lo, t_hi = ms->range_hi;
 
     if (warp == 0) {
         // ================================================== scheduler warp
         uint32_t it = 0, q_n = 0;
         int32_t seg_lo = 0, seg_hi = 0, seg_b = -1;  // last sequence found: [lo, hi)
-        for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
+        // What the K/V tile holds after the previous token's last tile: kind,
+        // sequence, token, ring base or box row, highest window row present
+        // (ring), compressed rows on top (ring).
+        int32_t bs_kind = -1, bs_seg = -1, bs_t = -1, bs_row0 = 0, bs_hi = 0, bs_top = 0;
+        for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
             const uint32_t slot = it & 1;
             // the slot's key list is rewritten only once every consumer is done
             bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
             if (!__all_sync(0xffffffffu, ok)) break;
             int32_t *list = reinterpret_cast<int32_t *>(smem + kOffList) + slot * kMaxList;
-            TokenInfo ti{t, 0, 0, 0, 0, 0, 0, 0};
+            TokenInfo ti = {};
+            ti.t = t;
+            ti.single = -1;
+            ti.b0 = -1;
             // tokens of a CTA increase, so the last sequence usually still holds t
             if (seg_b < 0 || t < seg_lo || t >= seg_hi) {
                 seg_b = find_segment(a.cu_q, a.batch, t);
@@ -310,17 +501,20 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const int32_t b = seg_b;
             if (b < 0) {
                 if (lane == 0) report_error(a.err, kErrCheck, kKerMla, 1);
+                bs_kind = -1;
             } else {
                 const int32_t seg0 = max(seg_lo, 0);
                 const int32_t pos = t - seg0;
+                ti.pos = pos;
+                ti.seg = b;
                 ti.win_start = max(t - a.window + 1, seg0);
                 ti.n_win = t - ti.win_start + 1;
-                int32_t n_cmp = 0;
+                int32_t n_cmp = 0, cbase = 0, vis = 0;
                 bool run = true;
                 if (use_cmp) {
-                    const int32_t cbase = __ldg(a.cu_c + b);
+                    cbase = __ldg(a.cu_c + b);
                     const int32_t seg_blocks = __ldg(a.cu_c + b + 1) - cbase;
-                    int32_t vis = min((pos + 1) / a.cmp_ratio, seg_blocks);
+                    vis = min((pos + 1) / a.cmp_ratio, seg_blocks);
                     if (cbase < 0 || vis < 0 || (int64_t)cbase + vis > a.Tc) {
                         if (lane == 0) report_error(a.err, kErrCheck, kKerMla, 2);
                         vis = 0;
@@ -358,52 +552,99 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         ti.cmp_first = cbase;
                     }
                 }
+                // every visible block, in order (the top-k kept them all)?
+                const bool allvis = run && n_cmp == vis && (n_cmp == 0 || ti.cmp_first == cbase);
+                ti.cbase = cbase;
                 ti.n_cmp = n_cmp;
-                const int32_t n_keys = ti.n_win + n_cmp;
-                if (n_keys <= kTileKeys) {
-                    ti.flags = kFlagMixed;
+                ti.flags = (run ? kFlagRun : 0) | (allvis ? kFlagAllVis : 0);
+                // Ring base, fixed by the position: a token at an odd position
+                // starts the ring at its own window start; one at an even
+                // position keeps the base of the position before it (its own
+                // window is then that one plus its row).
+                const bool ring_ok = a.window <= kTileKeys;
+                if (ring_ok) ti.b0 = (pos & 1) ? ti.win_start : max(t - a.window, seg0);
+                if (ti.n_win + n_cmp <= kTileKeys) {
                     ti.n_tiles = 1;
+                    if (ring_ok && (n_cmp == 0 || (allvis && ti.win_start == seg0))) {
+                        ti.single = kRing;  // window in slots [0, pos], blocks on top
+                        ti.n_top = n_cmp;
+                    } else {
+                        ti.single = kGMix;
+                    }
                 } else {
-                    ti.flags = run ? kFlagCmpRun : 0;
-                    ti.n_tiles = (ti.n_win + kTileKeys - 1) / kTileKeys +
-                                 (n_cmp + kTileKeys - 1) / kTileKeys;
+                    ti.n_wt = ring_ok ? 1 : (ti.n_win + kTileKeys - 1) / kTileKeys;
+                    ti.n_ct = (n_cmp + kTileKeys - 1) / kTileKeys;
+                    ti.n_tiles = ti.n_wt + ti.n_ct;
                 }
                 ti.valid = 1;
+                // Take over the previous token's last tile when it is this
+                // token's first one, loading only what it lacks.
+                const int32_t first_nat = tile_nat(ti, 0);
+                const TileDesc f = tile_at(ti, first_nat);
+                if (bs_t == t - 1 && bs_seg == b && bs_kind == f.kind && bs_row0 == f.row0) {
+                    if (f.kind == kRing && bs_hi >= t - 1 && f.n_valid <= bs_top + 1) {
+                        int32_t nd = 0;
+                        if (t > bs_hi) {  // this token's own row
+                            ti.d_row[nd] = t;
+                            ti.d_slot[nd] = (t - f.row0) & (kTileKeys - 1);
+                            ti.d_cmp[nd] = 0;
+                            ++nd;
+                        }
+                        if (f.n_valid > bs_top) {  // a block that just became visible
+                            ti.d_row[nd] = ti.cmp_first + bs_top;
+                            ti.d_slot[nd] = kTileKeys - 1 - bs_top;
+                            ti.d_cmp[nd] = 1;
+                            ++nd;
+                        }
+                        ti.reuse = 1;
+                        ti.n_delta = nd;
+                    } else if (f.kind == kCmpBox) {
+                        ti.reuse = 1;  // the box already holds the later blocks
+                    }
+                }
+                // state after this token: its last tile
+                const int32_t last_nat = tile_nat(ti, ti.n_tiles - 1);
+                const TileDesc l = tile_at(ti, last_nat);
+                if (l.kind == kRing) {
+                    int32_t hi;
+                    if (last_nat == first_nat && ti.reuse) hi = max(bs_hi, t);
+                    else hi = ring_box(ti, l) ? l.row0 + kTileKeys - 1 : t;  // box / gather
+                    if (l.n_valid > 0) hi = min(hi, t);  // later slots may hold blocks
+                    bs_kind = kRing;
+                    bs_hi = hi;
+                    bs_top = l.n_valid;
+                } else {
+                    bs_kind = l.kind == kCmpBox ? kCmpBox : -1;
+                    bs_hi = 0;
+                    bs_top = 0;
+                }
+                bs_seg = b;
+                bs_t = t;
+                bs_row0 = l.row0;
             }
             __syncwarp();  // list writes before the release below
             if (lane == 0) {
                 ms->info[slot] = ti;
                 tc::mbar_arrive(&ms->info_full[slot]);
-                // Q of this CTA's next token streams from HBM into L2 while
-                // this token runs; its TMA load then hits L2.
-                const int32_t tn = token_at(it + 1);
-                if (tn < a.T) tc::prefetch_l2_bulk(a.q + (int64_t)tn * a.H * 512, (uint32_t)a.H * 1024u);
+                // Q of the next token streams from HBM into L2 while this token
+                // runs; its TMA load then hits L2.
+                if (t + 1 < t_hi)
+                    tc::prefetch_l2_bulk(a.q + (int64_t)(t + 1) * a.H * 512, (uint32_t)a.H * 1024u);
             }
             if (!ti.valid) continue;
-            // Q rows of token t (H rows of 512; rows >= H stay zero), one pair
-            // of 64-wide chunks at a time as the previous token frees them
-            bool qbroke = false;
-            for (int pr = 0; pr < 4; ++pr) {
-                ok = cx.wait(&ms->q_empty[pr], (q_n & 1) ^ 1, 11);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    qbroke = true;
-                    break;
-                }
-                if (lane == 0) {
-                    tc::mbar_expect_tx(&ms->q_full[pr], 2u * a.H * 128u);
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * pr + cc;
-                        tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full[pr], 64 * c, 0,
-                                        t);
-                    }
-                }
+            // Q rows of token t (H rows of 512; rows >= H stay zero), once the
+            // previous token's last S^T has read its Q
+            ok = cx.wait(&ms->q_empty, (q_n & 1) ^ 1, 11);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) {
+                tc::mbar_expect_tx(&ms->q_full, 8u * a.H * 128u);
+                for (int c = 0; c < 8; ++c)
+                    tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full, 64 * c, 0, t);
             }
-            if (qbroke) break;
             ++q_n;
         }
         if (lane == 0 && q_n > 0)  // drain: every Q copy issued has landed
-            for (int pr = 0; pr < 4; ++pr)
-                if (!tc::mbar_wait(&ms->q_full[pr], (q_n - 1) & 1)) cx.fail(13);
+            if (!tc::mbar_wait(&ms->q_full, (q_n - 1) & 1)) cx.fail(13);
     } else if (warp == 1 || warp == 2) {
         // ==================================================== loader warps
         // Gathered tiles: thread i covers, for slab s, the 16-byte column
@@ -412,34 +653,63 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // coalesced run. Row addresses are computed once per tile.
         const int li = tid - 32;  // 0..63
         const int col = li & 15, sgrp = li >> 4;
-        uint32_t it = 0, kv_n = 0;
+        // kf_n counts the tiles loaded into. Both K/V barriers advance once
+        // per loaded tile: kv_full when it has landed, kv_empty when the
+        // tensor core has finished with the tile before it. A tile taken over
+        // whole from the previous token loads nothing and touches neither, so
+        // the parity waits below never fall more than one phase behind.
+        uint32_t it = 0, kf_n = 0;
         const uint32_t kv_base = tc::smem_u32(smem + kOffKV);
         bool stop = false;
-        for (int32_t t = token_at(it); t < a.T && !stop; t = token_at(++it)) {
+        for (int32_t t = t_lo; t < t_hi && !stop; ++t, ++it) {
             const uint32_t slot = it & 1;
             if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40)) break;
-            const TokenInfo ti = ms->info[slot];
+            const TokenInfo &ti = ms->info[slot];  // released after this token's loads
             const int32_t *list = reinterpret_cast<const int32_t *>(smem + kOffList) + slot * kMaxList;
-            for (int32_t j = 0; j < ti.n_tiles && !stop; ++j, ++kv_n) {
-                const TileDesc td = tile_desc(ti, j);
-                if (td.kind != kTileGather) {
-                    const CUtensorMap *map = td.kind == kTileOri ? &ori_map : &cmp_map;
+            const int32_t n_tiles = ti.valid ? ti.n_tiles : 0;
+            for (int32_t j = 0; j < n_tiles && !stop; ++j) {
+                if (j == 0 && ti.reuse) {
+                    if (ti.n_delta == 0) continue;
+                    // the missing rows: 16 threads per row, 256 B per slab
+                    const int dr = li >> 4;
                     for (int s = 0; s < 4; ++s) {
-                        if (!cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 41)) {
+                        if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 44)) {
+                            stop = true;
+                            break;
+                        }
+                        if (dr < ti.n_delta) {
+                            const int c16 = 16 * s + col;
+                            const int chunk = c16 >> 3, w = c16 & 7;
+                            const int k = ti.d_slot[dr];
+                            const __nv_bfloat16 *src =
+                                (ti.d_cmp[dr] ? a.cmp_kv : a.ori_kv) + (int64_t)ti.d_row[dr] * 512;
+                            cp_async16(kv_base + chunk * 16384 + k * 128 + ((w ^ (k & 7)) << 4),
+                                       src + c16 * 8);
+                        }
+                    }
+                    if (!stop) cp_async_arrive(&ms->kv_full);
+                    ++kf_n;
+                    continue;
+                }
+                const TileDesc td = tile_at(ti, tile_nat(ti, j));
+                if (td.kind == kWinBox || td.kind == kCmpBox || ring_box(ti, td)) {
+                    const CUtensorMap *map = td.kind == kCmpBox ? &cmp_map : &ori_map;
+                    for (int s = 0; s < 4; ++s) {
+                        if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 41)) {
                             stop = true;
                             break;
                         }
                         if (li == 0) {
-                            tc::mbar_expect_tx(&ms->kv_full[s], 32768u);
+                            if (s == 0) tc::mbar_expect_tx(&ms->kv_full, 131072u);
                             for (int cc = 0; cc < 2; ++cc) {
                                 const int c = 2 * s + cc;
-                                tc::tma_load_2d(smem + kOffKV + c * 16384, map, &ms->kv_full[s],
+                                tc::tma_load_2d(smem + kOffKV + c * 16384, map, &ms->kv_full,
                                                 64 * c, td.row0);
                             }
-                        } else {
-                            tc::mbar_arrive(&ms->kv_full[s]);
                         }
                     }
+                    if (!stop && li != 0) tc::mbar_arrive(&ms->kv_full);
+                    ++kf_n;
                     continue;
                 }
                 // gathered tile: this thread's 32 slots
@@ -447,14 +717,27 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                 for (int m = 0; m < 32; ++m) {
                     const int k = sgrp + 4 * m;
-                    const int32_t e = td.key0 + k;
                     const __nv_bfloat16 *p = nullptr;
-                    if (k < td.n_valid) {
-                        if (e < ti.n_win) {
-                            p = a.ori_kv + (int64_t)(ti.win_start + e) * 512;
+                    if (td.kind == kRing) {
+                        if (k >= kTileKeys - td.n_valid) {
+                            p = a.cmp_kv + (int64_t)(ti.cmp_first + (kTileKeys - 1 - k)) * 512;
                         } else {
-                            const int32_t ce = e - ti.n_win;
-                            p = a.cmp_kv + (int64_t)(a.cmp_idx ? list[ce] : ti.cmp_first + ce) * 512;
+                            const int32_t r = ti.t - ((ti.t - td.row0 - k) & (kTileKeys - 1));
+                            if (r >= ti.win_start) p = a.ori_kv + (int64_t)r * 512;
+                        }
+                    } else if (td.kind == kGather) {
+                        if (k < td.n_valid) {
+                            const int32_t e = td.e0 + k;
+                            const int32_t row = (ti.flags & kFlagRun) ? ti.cmp_first + e : list[e];
+                            p = a.cmp_kv + (int64_t)row * 512;
+                        }
+                    } else {  // kGMix: window rows, then compressed entries
+                        if (k < ti.n_win) {
+                            p = a.ori_kv + (int64_t)(ti.win_start + k) * 512;
+                        } else if (k < ti.n_win + ti.n_cmp) {
+                            const int32_t e = k - ti.n_win;
+                            const int32_t row = (ti.flags & kFlagRun) ? ti.cmp_first + e : list[e];
+                            p = a.cmp_kv + (int64_t)row * 512;
                         }
                     }
                     src[m] = p;
@@ -463,7 +746,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 // itself once this thread's copies land; the thread goes on to
                 // the next slab without waiting.
                 for (int s = 0; s < 4; ++s) {
-                    if (!cx.wait(&ms->kv_empty[s], (kv_n & 1) ^ 1, 42)) {
+                    if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 42)) {
                         stop = true;
                         break;
                     }
@@ -476,16 +759,16 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             cp_async16(kv_base + chunk * 16384 + k * 128 + ((w ^ (k & 7)) << 4),
                                        src[m] + c16 * 8);
                     }
-                    cp_async_arrive(&ms->kv_full[s]);
                 }
+                if (!stop) cp_async_arrive(&ms->kv_full);
+                ++kf_n;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
         }
         cp_async_wait_all();  // drain: no copy outlives the CTA
-        if (li == 0 && kv_n > 0)  // and no TMA copy either (last tile's phases)
-            for (int s = 0; s < 4; ++s)
-                if (!tc::mbar_wait(&ms->kv_full[s], (kv_n - 1) & 1)) cx.fail(43);
+        if (li == 0 && kf_n > 0)  // and no TMA copy either (last loaded tile's phase)
+            if (!tc::mbar_wait(&ms->kv_full, (kf_n - 1) & 1)) cx.fail(43);
     } else if (warp == 3) {
         // ========================================================= MMA warp
         if (lane == 0) {
@@ -497,46 +780,60 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const uint64_t ds_b = tc::smem_desc(tc::smem_u32(smem + kOffQ), 16, 1024);
             const uint64_t do_a = tc::smem_desc(tc::smem_u32(smem + kOffKV), 16384, 1024);
             const uint64_t do_b = tc::smem_desc(tc::smem_u32(smem + kOffP), 16384, 1024);
-            uint32_t it = 0, q_n = 0, kv_n = 0, p_n = 0;
+            uint32_t it = 0, q_n = 0, kf_n = 0, p_n = 0;
             bool issued = false;
-            for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
+            for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
                 const uint32_t slot = it & 1;
                 if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
-                const TokenInfo ti = ms->info[slot];
+                const int32_t n_tiles = ms->info[slot].valid ? ms->info[slot].n_tiles : 0;
+                // a first tile taken over whole needs no load
+                const bool first_loaded = !(ms->info[slot].reuse && ms->info[slot].n_delta == 0);
                 tc::mbar_arrive(&ms->info_empty[slot]);
-                if (!ti.valid) continue;
+                if (n_tiles == 0) continue;
                 bool stop = false;
-                for (int32_t j = 0; j < ti.n_tiles && !stop; ++j, ++kv_n) {
-                    for (int s = 0; s < 4; ++s) {
-                        if ((j == 0 && !cx.wait(&ms->q_full[s], q_n & 1, 21)) ||
-                            !cx.wait(&ms->kv_full[s], kv_n & 1, 22)) {
-                            stop = true;
-                            break;
-                        }
-                        // slabs gathered by cp.async were written through the
-                        // generic proxy: order them before the tensor core's reads
-                        tc::fence_proxy_async_smem();
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int c = 2 * s + cc;
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_bf16(tmem + kColS, tc::desc_add(ds_a, c * 16384 + kk * 32),
-                                             tc::desc_add(ds_b, c * 8192 + kk * 32), id_s,
-                                             (c | kk) != 0);
-                        }
-                        issued = true;
-                        // the last tile's S^T frees this pair of Q chunks
-                        if (j == ti.n_tiles - 1) tc::mma_commit(&ms->q_empty[s]);
+                for (int32_t j = 0; j < n_tiles && !stop; ++j) {
+                    const bool loaded = j > 0 || first_loaded;
+                    // Q (first tile) and the whole tile, then all 32 S^T MMAs
+                    // back to back: issuing slab by slab, between barrier
+                    // checks, runs the tensor core at about half speed.
+                    if ((j == 0 && !cx.wait(&ms->q_full, q_n & 1, 21)) ||
+                        (loaded && !cx.wait(&ms->kv_full, kf_n & 1, 22))) {
+                        stop = true;
+                        break;
                     }
-                    if (stop) break;
+                    // slabs gathered by cp.async were written through the
+                    // generic proxy: order them before the tensor core's reads
+                    tc::fence_proxy_async_smem();
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_bf16(tmem + kColS, tc::desc_add(ds_a, c * 16384 + kk * 32),
+                                         tc::desc_add(ds_b, c * 8192 + kk * 32), id_s, (c | kk) != 0);
+                    issued = true;
+                    // the last tile's S^T frees Q
+                    if (j == n_tiles - 1) tc::mma_commit(&ms->q_empty);
+                    if (loaded) ++kf_n;
                     tc::mma_commit(&ms->s_full);
                     if (!cx.wait(&ms->p_full, p_n & 1, 23)) {
                         stop = true;
                         break;
                     }
                     ++p_n;
+                    // The K/V tile is handed back to the loaders only when the
+                    // next tile loads into it: the next token's info decides
+                    // for this token's last tile.
+                    bool release = true;
+                    if (j == n_tiles - 1 && t + 1 < t_hi) {
+                        const uint32_t ns = (it + 1) & 1;
+                        if (!cx.wait(&ms->info_full[ns], ((it + 1) >> 1) & 1, 25)) {
+                            stop = true;
+                            break;
+                        }
+                        const TokenInfo &nx = ms->info[ns];
+                        release = !(nx.valid && nx.reuse && nx.n_delta == 0);
+                    }
                     tc::tc_fence_after();
                     for (int s = 0; s < 4; ++s) {
 #pragma unroll
@@ -544,7 +841,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             tc::mma_bf16(tmem + kColO + 64 * s,
                                          tc::desc_add(do_a, 2 * s * 16384 + kk * 2048),
                                          tc::desc_add(do_b, kk * 2048), id_o, (j > 0 || kk > 0));
-                        tc::mma_commit(&ms->kv_empty[s]);
+                        if (release) tc::mma_commit(&ms->kv_empty[s]);
                     }
                 }
                 if (stop) break;
@@ -572,14 +869,16 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         unsigned char *pbuf = smem + kOffP;
         const float c = a.softmax_scale * kLog2e;
         uint32_t it = 0, s_n = 0, o_n = 0, tile_ctr = 0;
-        for (int32_t t = token_at(it); t < a.T; t = token_at(++it)) {
+        for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
             if (!bar_red_and(bar_id, ok)) break;
-            const TokenInfo ti = ms->info[slot];
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
-            if (!ti.valid) continue;
+            const TokenInfo &ti = ms->info[slot];  // released at the end of the token
+            if (!ti.valid) {
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
+                continue;
+            }
             // Per-head scalars live one head per lane (head h0 + lane):
             // m_lane the running max (base 2); m_cur[] is every thread's copy
             // of all 32, refreshed by shuffles only when some max moves.
@@ -601,7 +900,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 float v[32];
                 tc::tmem_ld32(lane_addr + kColS + h0, v);
                 tc::tmem_wait_ld();
-                const bool key_ok = row < tile_desc(ti, j).n_valid;
+                const bool key_ok = slot_valid(ti, tile_at(ti, tile_nat(ti, j)), row);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
                 // A head's max moves only when some score of this tile exceeds
@@ -706,6 +1005,8 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 for (int i = 0; i < 32; ++i)
                     if (i < n_h) outp[(int64_t)i * 512 + 128 * sl] = __float2bfloat16_rn(x[i] * il[i]);
             }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
             tc::tc_fence_before();
         }
     }
@@ -738,8 +1039,7 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t runs = ((int64_t)a.T + kChunk - 1) / kChunk;
-    const int ctas = runs < sms ? (int)runs : sms;
+    const int ctas = a.T < sms ? a.T : sms;
     sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, a);
     return cudaGetLastError();
 }
