@@ -480,6 +480,18 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // sequence, token, ring base or box row, highest window row present
         // (ring), compressed rows on top (ring).
         int32_t bs_kind = -1, bs_seg = -1, bs_t = -1, bs_row0 = 0, bs_hi = 0, bs_top = 0;
+        // The first 512 index entries of the next token, loaded one token
+        // ahead so that their latency hides behind the wait for a free slot.
+        int32_t jn[16];
+        auto load_first_round = [&](int32_t tt) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int32_t e = 32 * r + lane;
+                jn[r] = (a.cmp_idx && tt < t_hi && e < a.topk) ? __ldg(a.cmp_idx + (int64_t)tt * a.topk + e)
+                                                               : -1;
+            }
+        };
+        load_first_round(t_lo);
         for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
             const uint32_t slot = it & 1;
             // the slot's key list is rewritten only once every consumer is done
@@ -528,7 +540,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                             for (int r = 0; r < 16; ++r) {
                                 const int32_t e = e0 + 32 * r + lane;
-                                jv[r] = e < a.topk ? __ldg(row + e) : -1;
+                                jv[r] = e0 == 0 ? jn[r] : (e < a.topk ? __ldg(row + e) : -1);
                             }
 #pragma unroll
                             for (int r = 0; r < 16; ++r) {
@@ -631,7 +643,10 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (t + 1 < t_hi)
                     tc::prefetch_l2_bulk(a.q + (int64_t)(t + 1) * a.H * 512, (uint32_t)a.H * 1024u);
             }
-            if (!ti.valid) continue;
+            if (!ti.valid) {
+                load_first_round(t + 1);
+                continue;
+            }
             // Q rows of token t (H rows of 512; rows >= H stay zero), once the
             // previous token's last S^T has read its Q
             ok = cx.wait(&ms->q_empty, (q_n & 1) ^ 1, 11);
@@ -642,6 +657,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full, 64 * c, 0, t);
             }
             ++q_n;
+            load_first_round(t + 1);
         }
         if (lane == 0 && q_n > 0)  // drain: every Q copy issued has landed
             if (!tc::mbar_wait(&ms->q_full, (q_n - 1) & 1)) cx.fail(13);
@@ -901,15 +917,21 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 tc::tmem_ld32(lane_addr + kColS + h0, v);
                 tc::tmem_wait_ld();
                 const bool key_ok = slot_valid(ti, tile_at(ti, tile_nat(ti, j)), row);
+                // v = scaled score - running max (base 2), -inf off the keys
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
+                for (int i = 0; i < 32; ++i) v[i] = key_ok ? fmaf(v[i], c, -m_cur[i]) : -INFINITY;
                 // A head's max moves only when some score of this tile exceeds
                 // it by more than kLazyMax; the warpgroup first checks whether
                 // any does, and only then reduces the tile maxima.
                 bool exceeds = false;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) exceeds |= v[i] > m_cur[i] + kLazyMax;
+                for (int i = 0; i < 32; ++i) exceeds |= v[i] > kLazyMax;
                 if (bar_red_or(bar_id, exceeds)) {
+                    // the scaled scores again (S^T is still in tensor memory)
+                    tc::tmem_ld32(lane_addr + kColS + h0, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
                     // tile max per head: warp maxima (one head per lane) across the
                     // four lane quarters; every warp derives the same lazy update
                     const uint32_t rs = tile_ctr & 1;
@@ -945,6 +967,8 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             tc::tmem_wait_st();
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] -= m_cur[i];
                 }
                 // Probabilities -> P^T row `row`, heads h0..h0+31 (64 B of the
                 // 128-byte MN-major SW128 row: 16-byte chunks 4 wg .. 4 wg + 3).
@@ -956,8 +980,8 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = 8 * cq + 2 * e;
-                        const float p0 = tc::ex2_approx(v[i] - m_cur[i]);
-                        const float p1 = tc::ex2_approx(v[i + 1] - m_cur[i + 1]);
+                        const float p0 = tc::ex2_approx(v[i]);
+                        const float p1 = tc::ex2_approx(v[i + 1]);
                         lp[i] += p0;
                         lp[i + 1] += p1;
                         __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
