@@ -26,6 +26,10 @@
 //     epilogue warps selects one token's top-k with a warp-level 4-pass 8-bit
 //     radix select on order-preserving keys and emits the winners in row
 //     order with warp scans.
+//   * A token that sees at most topk blocks selects all of them whatever
+//     their scores, so unless the caller asks for the values it is not scored
+//     at all (its row is written by the selection's n <= k path); a group
+//     with no token left to score loads and multiplies nothing.
 //   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
 //     and selection. Every mbarrier wait is bounded.
 #include "common.cuh"
@@ -250,15 +254,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             gi.spill = 0;
             gi.valid = 1;
             int32_t segs[kG];
+            bool scored[kG];
 #pragma unroll
             for (int g = 0; g < kG; ++g) {
+                scored[g] = false;
                 const int32_t t = gi.t0 + g;
                 gi.nv[g] = 0;
                 gi.cb[g] = 0;
                 gi.pass[g] = Pass{0, 0, 0, 0};
                 segs[g] = -1;
                 if (t >= a.T) continue;
-                const int32_t b = find_segment(a.cu_q, a.batch, t);
+                // consecutive tokens: the previous token's sequence usually holds t
+                int32_t b = -1;
+                if (g > 0 && segs[g - 1] >= 0 && t < __ldg(a.cu_q + segs[g - 1] + 1))
+                    b = segs[g - 1];
+                else
+                    b = find_segment(a.cu_q, a.batch, t);
                 if (b < 0) {
                     if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 1);
                     continue;
@@ -274,14 +285,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 gi.nv[g] = nv;
                 gi.cb[g] = cbase;
-                if (nv > kScoreCap) gi.spill = 1;
+                // A token that sees at most topk blocks keeps all of them,
+                // whatever their scores: it is scored only if the caller
+                // asked for the values.
+                scored[g] = nv > 0 && (a.topk_val != nullptr || nv > a.topk);
+                if (scored[g] && nv > kScoreCap) gi.spill = 1;
             }
             // one pass per run of tokens sharing a sequence
 #pragma unroll
             for (int g = 0; g < kG; ++g) {
-                if (segs[g] < 0 || gi.nv[g] == 0) continue;
+                if (segs[g] < 0 || !scored[g]) continue;
                 const bool joins = g > 0 && gi.n_pass > 0 && segs[g - 1] == segs[g] &&
-                                   gi.nv[g - 1] > 0;
+                                   scored[g - 1];
                 if (joins) {
                     Pass &p = gi.pass[gi.n_pass - 1];
                     p.mask |= 1 << g;
@@ -413,8 +428,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 sc = sc_smem;
                 sc_stride = kScoreCap;
             }
-            // weights of the group's tokens (0 beyond Hi / T)
-            for (int i = ltid; i < kG * 64; i += 128) {
+            // weights of the group's tokens (0 beyond Hi / T), if any is scored
+            for (int i = ltid; gi.n_pass > 0 && i < kG * 64; i += 128) {
                 const int g = i >> 6, h = i & 63;
                 const int32_t t = gi.t0 + g;
                 ms->w[i] = (h < a.Hi && t < a.T) ? __ldg(a.w + (int64_t)t * a.Hi + h) : 0.0f;
