@@ -43,6 +43,19 @@ __device__ __forceinline__ int32_t find_segment(const int32_t *__restrict__ cu, 
     return lo;
 }
 
+// The same lookup over offsets already staged in shared memory.
+__device__ __forceinline__ int32_t find_segment_smem(const int32_t *cu, int32_t batch, int32_t t) {
+    int32_t lo = 0, hi = batch;
+    if (batch <= 0 || t < cu[0]) return -1;
+    while (lo < hi) {
+        int32_t mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    if (lo >= batch || cu[lo + 1] <= t) return -1;
+    return lo;
+}
+
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 maps
 // like +0 so that equal scores are equal keys.
 __device__ __forceinline__ uint32_t float_key(float s) {

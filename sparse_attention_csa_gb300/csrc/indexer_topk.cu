@@ -46,6 +46,7 @@ constexpr int kG = 4;               // tokens per group
 constexpr int kTileRows = 128;      // compressed rows per MMA tile
 constexpr int kScoreCap = 5120;     // rows per token kept in shared memory
 constexpr int kMaxCtas = 1024;      // persistent grid bound (sizes the scratch)
+constexpr int kCuCap = 500;         // sequences whose offsets are staged in shared memory
 
 // shared memory map (1024-aligned base)
 constexpr uint32_t kOffB = 0;                 // q group: 2 chunks x [256 rows x 128 B]
@@ -75,9 +76,11 @@ struct Misc {
     GroupInfo info[2];
     float w[kG * 64];
     int32_t hist[4][256];
+    int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
 };
 
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool bar_red_and(bool v) {
     uint32_t out;
@@ -231,6 +234,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         ms->abort = 0;
         tc::fence_mbar_init();
     }
+    // The producer looks up every token's sequence: keep the offsets on chip.
+    const bool cu_smem = a.batch <= kCuCap;
+    if (cu_smem)
+        for (int i = tid; i <= a.batch; i += kThreads) {
+            ms->cu_q[i] = __ldg(a.cu_q + i);
+            ms->cu_c[i] = a.Tc > 0 ? __ldg(a.cu_c + i) : 0;
+        }
     if (warp == 1) {
         tc::tmem_alloc(&ms->tmem_base, 512);
         tc::tmem_relinquish();
@@ -247,49 +257,51 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     if (warp == 0) {
         // ===================================================== producer warp
         uint32_t it = 0, b_n = 0, a_n = 0;
-        for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+        bool quit = false;
+        for (int32_t grp = blockIdx.x; grp < n_groups && !quit; grp += gridDim.x) {
             GroupInfo gi;
             gi.t0 = grp * kG;
             gi.n_pass = 0;
             gi.spill = 0;
             gi.valid = 1;
+            // Lane g < kG works out token t0 + g; the warp then shares the results.
+            int32_t my_seg = -1, my_nv = 0, my_cb = 0;
+            bool my_scored = false;
+            {
+                const int32_t t = gi.t0 + lane;
+                if (lane < kG && t < a.T) {
+                    const int32_t *cq = cu_smem ? ms->cu_q : a.cu_q;
+                    const int32_t *cc = cu_smem ? ms->cu_c : a.cu_c;
+                    my_seg = cu_smem ? find_segment_smem(cq, a.batch, t) : find_segment(cq, a.batch, t);
+                    if (my_seg < 0) {
+                        report_error(a.err, kErrCheck, kKerIndexer, 1);
+                    } else if (a.Tc > 0) {
+                        const int32_t pos = t - cq[my_seg];
+                        const int32_t cbase = cc[my_seg];
+                        int32_t nv = min((pos + 1) / a.cmp_ratio, cc[my_seg + 1] - cbase);
+                        if (cbase < 0 || nv < 0 || (int64_t)cbase + nv > a.Tc) {
+                            report_error(a.err, kErrCheck, kKerIndexer, 2);
+                            nv = 0;
+                        }
+                        my_nv = nv;
+                        my_cb = cbase;
+                        // A token that sees at most topk blocks keeps all of
+                        // them, whatever their scores: it is scored only if the
+                        // caller asked for the values.
+                        my_scored = nv > 0 && (a.topk_val != nullptr || nv > a.topk);
+                    }
+                }
+            }
             int32_t segs[kG];
             bool scored[kG];
 #pragma unroll
             for (int g = 0; g < kG; ++g) {
-                scored[g] = false;
-                const int32_t t = gi.t0 + g;
-                gi.nv[g] = 0;
-                gi.cb[g] = 0;
+                segs[g] = __shfl_sync(0xffffffffu, my_seg, g);
+                gi.nv[g] = __shfl_sync(0xffffffffu, my_nv, g);
+                gi.cb[g] = __shfl_sync(0xffffffffu, my_cb, g);
+                scored[g] = __shfl_sync(0xffffffffu, my_scored ? 1 : 0, g) != 0;
                 gi.pass[g] = Pass{0, 0, 0, 0};
-                segs[g] = -1;
-                if (t >= a.T) continue;
-                // consecutive tokens: the previous token's sequence usually holds t
-                int32_t b = -1;
-                if (g > 0 && segs[g - 1] >= 0 && t < __ldg(a.cu_q + segs[g - 1] + 1))
-                    b = segs[g - 1];
-                else
-                    b = find_segment(a.cu_q, a.batch, t);
-                if (b < 0) {
-                    if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 1);
-                    continue;
-                }
-                segs[g] = b;
-                if (a.Tc == 0) continue;
-                const int32_t pos = t - __ldg(a.cu_q + b);
-                const int32_t cbase = __ldg(a.cu_c + b);
-                int32_t nv = min((pos + 1) / a.cmp_ratio, __ldg(a.cu_c + b + 1) - cbase);
-                if (cbase < 0 || nv < 0 || (int64_t)cbase + nv > a.Tc) {
-                    if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 2);
-                    nv = 0;
-                }
-                gi.nv[g] = nv;
-                gi.cb[g] = cbase;
-                // A token that sees at most topk blocks keeps all of them,
-                // whatever their scores: it is scored only if the caller
-                // asked for the values.
-                scored[g] = nv > 0 && (a.topk_val != nullptr || nv > a.topk);
-                if (scored[g] && nv > kScoreCap) gi.spill = 1;
+                if (scored[g] && gi.nv[g] > kScoreCap) gi.spill = 1;
             }
             // one pass per run of tokens sharing a sequence
 #pragma unroll
@@ -313,6 +325,30 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (lane == 0) report_error(a.err, kErrCheck, kKerIndexer, 3);
                 gi.valid = 0;
             }
+            if (!gi.valid || gi.n_pass == 0) {
+                // Nothing to score: each token keeps all its visible blocks
+                // (none when invalid). This warp writes the rows itself and the
+                // group never reaches the other roles.
+                const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
+                for (int g = 0; g < kG; ++g) {
+                    const int32_t t = gi.t0 + g;
+                    if (t >= a.T) break;
+                    const int32_t n = gi.valid ? gi.nv[g] : 0, cb = gi.cb[g];
+                    int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
+                    if (vec) {  // 16-byte stores: four entries per lane
+                        for (int32_t i = 4 * lane; i < a.topk; i += 128)
+                            *reinterpret_cast<int4 *>(idx_row + i) =
+                                make_int4(i < n ? cb + i : -1, i + 1 < n ? cb + i + 1 : -1,
+                                          i + 2 < n ? cb + i + 2 : -1, i + 3 < n ? cb + i + 3 : -1);
+                    } else {
+                        for (int32_t i = lane; i < a.topk; i += 32) idx_row[i] = i < n ? cb + i : -1;
+                    }
+                    if (a.topk_val)  // only rows with no visible block get here
+                        for (int32_t i = lane; i < a.topk; i += 32)
+                            a.topk_val[(int64_t)t * a.topk + i] = -INFINITY;
+                }
+                continue;
+            }
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -320,7 +356,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 ms->info[slot] = gi;
                 tc::mbar_arrive(&ms->info_full[slot]);
             }
-            if (!gi.valid || gi.n_pass == 0) continue;
+            ++it;
             // q rows of the group (4 tokens x HPAD heads; missing rows read as 0)
             ok = cx.wait(&ms->b_empty, (b_n & 1) ^ 1, 11);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -349,7 +385,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     }
                 }
             }
-            if (broke) break;
+            if (broke) quit = true;
+        }
+        // end of the stream: a group with valid = -1 stops the other roles
+        if (!quit) {
+            const uint32_t slot = it & 1;
+            const bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 15);
+            if (__all_sync(0xffffffffu, ok) && lane == 0) {
+                ms->info[slot].valid = -1;
+                tc::mbar_arrive(&ms->info_full[slot]);
+            }
         }
         // drain: every copy issued has landed before the CTA exits
         if (lane == 0) {
@@ -365,11 +410,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const uint64_t db = tc::smem_desc(tc::smem_u32(smem + kOffB), 16, 1024);
             uint32_t it = 0, b_n = 0, a_n = 0, t_n = 0;
             bool issued = false;
-            for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+            for (;; ++it) {
                 const uint32_t slot = it & 1;
                 if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
                 const GroupInfo gi = ms->info[slot];
                 tc::mbar_arrive(&ms->info_empty[slot]);
+                if (gi.valid < 0) break;
                 if (!gi.valid || gi.n_pass == 0) continue;
                 if (!cx.wait(&ms->b_full, b_n & 1, 21)) break;
                 ++b_n;
@@ -413,12 +459,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
         uint32_t it = 0, t_n = 0;
-        for (int32_t grp = blockIdx.x; grp < n_groups; grp += gridDim.x, ++it) {
+        for (;; ++it) {
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
             if (!bar_red_and(ok)) break;
             // read in place; the slot is released at the end of the group
             const GroupInfo &gi = ms->info[slot];
+            if (gi.valid < 0) break;
             float *sc;
             int32_t sc_stride;
             if (gi.spill) {
