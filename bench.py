@@ -444,6 +444,8 @@ def run_ours(args, world, rank, local):
                                + f", H={spec.heads}, D={spec.dim}, window {spec.win_left + 1}",
                    "tokens_per_step": T, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between steps (256 MB write, outside the step events)",
+                   "indexer_values": "not requested: tokens whose visible blocks fit in top-k "
+                                     "keep them all unscored",
                    "wall_ms_incl_flush": wall * 1e3 / args.steps},
         "roofline": roof,
         "kernels_ms": avg,
