@@ -46,12 +46,14 @@
 //     thread per key = one TMEM lane, 32 head scores; epilogue: one thread per
 //     d row of O^T, so a warp's lanes hold 32 consecutive d of each head:
 //     64-byte stores with no data exchanged between lanes).
-//   * Online softmax in base 2 with a lazily moved running max: a head's max
-//     only moves when a tile exceeds it by more than 8 (a factor 256), so O^T
-//     in tensor memory is rescaled rarely, and the cross-lane reduction of the
-//     tile maxima runs only for tiles where some score exceeds a max by that
-//     much (a warpgroup-wide vote decides). Row sums accumulate per thread in
-//     fp32 and are reduced once per token.
+//   * Online softmax in base 2. The max starts as the exact maximum of the
+//     sink and the first tile (so the largest probability is exactly 1 in
+//     bf16, which keeps short key sets within the output bound); after that
+//     it moves lazily: only when a tile exceeds it by more than 8 (a factor
+//     256), so O^T in tensor memory is rescaled rarely, and the cross-lane
+//     reduction of the tile maxima runs only for tiles where some score
+//     exceeds a max by that much (a warpgroup-wide vote decides). Row sums
+//     accumulate per thread in fp32 and are reduced once per token.
 //   * Every mbarrier wait is bounded; a timeout records CSA_ERR_TIMEOUT, the
 //     CTA drains its copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -917,40 +919,60 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 tc::tmem_ld32(lane_addr + kColS + h0, v);
                 tc::tmem_wait_ld();
                 const bool key_ok = slot_valid(ti, tile_at(ti, tile_nat(ti, j)), row);
-                // v = scaled score - running max (base 2), -inf off the keys
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = key_ok ? fmaf(v[i], c, -m_cur[i]) : -INFINITY;
-                // A head's max moves only when some score of this tile exceeds
-                // it by more than kLazyMax; the warpgroup first checks whether
-                // any does, and only then reduces the tile maxima.
-                bool exceeds = false;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) exceeds |= v[i] > kLazyMax;
-                if (bar_red_or(bar_id, exceeds)) {
-                    // the scaled scores again (S^T is still in tensor memory)
-                    tc::tmem_ld32(lane_addr + kColS + h0, v);
-                    tc::tmem_wait_ld();
+                if (j == 0) {
+                    // A token's first tile sets the max exactly: the max of the
+                    // sink and the tile's scores, so the largest probability is
+                    // exactly 1 in bf16 (a single dominant key then carries no
+                    // rounding into P V). Row sums are still zero: nothing to scale.
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
-                    // tile max per head: warp maxima (one head per lane) across the
-                    // four lane quarters; every warp derives the same lazy update
                     const uint32_t rs = tile_ctr & 1;
                     ms->red[rs][q4][h0 + lane] = reduce_scatter32<true>(v, lane);
                     tc::named_bar_sync(bar_id, 128);
                     const float mt =
                         fmaxf(fmaxf(ms->red[rs][0][h0 + lane], ms->red[rs][1][h0 + lane]),
                               fmaxf(ms->red[rs][2][h0 + lane], ms->red[rs][3][h0 + lane]));
-                    const bool up = mt > m_lane + kLazyMax;
-                    const float al_lane =
-                        up ? (m_lane == -INFINITY ? 0.0f : tc::ex2_approx(m_lane - mt)) : 1.0f;
-                    if (up) m_lane = mt;
-                    if (__any_sync(0xffffffffu, up)) {  // uniform across the warpgroup
+                    m_lane = fmaxf(m_lane, mt);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
-                            lp[i] *= __shfl_sync(0xffffffffu, al_lane, i);
-                        }
-                        if (j > 0) {
+                    for (int i = 0; i < 32; ++i) {
+                        m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
+                        v[i] -= m_cur[i];
+                    }
+                } else {
+                    // v = scaled score - running max (base 2), -inf off the keys
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = key_ok ? fmaf(v[i], c, -m_cur[i]) : -INFINITY;
+                    // After the first tile a head's max moves only when some score
+                    // of a tile exceeds it by more than kLazyMax: the warpgroup
+                    // first checks whether any does, and only then reduces the
+                    // tile maxima.
+                    bool exceeds = false;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) exceeds |= v[i] > kLazyMax;
+                    if (bar_red_or(bar_id, exceeds)) {
+                        // the scaled scores again (S^T is still in tensor memory)
+                        tc::tmem_ld32(lane_addr + kColS + h0, v);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = key_ok ? v[i] * c : -INFINITY;
+                        // tile max per head: warp maxima (one head per lane) across the
+                        // four lane quarters; every warp derives the same lazy update
+                        const uint32_t rs = tile_ctr & 1;
+                        ms->red[rs][q4][h0 + lane] = reduce_scatter32<true>(v, lane);
+                        tc::named_bar_sync(bar_id, 128);
+                        const float mt =
+                            fmaxf(fmaxf(ms->red[rs][0][h0 + lane], ms->red[rs][1][h0 + lane]),
+                                  fmaxf(ms->red[rs][2][h0 + lane], ms->red[rs][3][h0 + lane]));
+                        const bool up = mt > m_lane + kLazyMax;
+                        const float al_lane =
+                            up ? (m_lane == -INFINITY ? 0.0f : tc::ex2_approx(m_lane - mt)) : 1.0f;
+                        if (up) m_lane = mt;
+                        if (__any_sync(0xffffffffu, up)) {  // uniform across the warpgroup
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
+                                lp[i] *= __shfl_sync(0xffffffffu, al_lane, i);
+                            }
                             // O^T of the earlier tiles is complete (the commit that
                             // signalled this S^T covers it); scale this half's columns.
 #pragma unroll 1
@@ -966,9 +988,9 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                             }
                             tc::tmem_wait_st();
                         }
-                    }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] -= m_cur[i];
+                        for (int i = 0; i < 32; ++i) v[i] -= m_cur[i];
+                    }
                 }
                 // Probabilities -> P^T row `row`, heads h0..h0+31 (64 B of the
                 // 128-byte MN-major SW128 row: 16-byte chunks 4 wg .. 4 wg + 3).

@@ -166,3 +166,34 @@ def test_full_size_sampled(name):
         check_attention(out[tk], lse[tk], ref_out, ref_lse, f"{name} layer {li}")
         del case
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("win_left", [300, 1023])
+def test_wide_window(win_left):
+    """Windows wider than one key tile (several window tiles per token, no ring)."""
+    lengths = [1200, 5, 300]
+    layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=64, index_heads=8, index_dim=64)
+    case = layer_cases(custom_spec(lengths, heads=16, win_left=win_left, layers=(layer,),
+                                   seed=win_left))[0]
+    idx = gpu_topk(case)
+    toks = sample_tokens(lengths, 4, n_random=24, cap=48, seed=5)
+    out, lse = gpu_attention(case, idx)
+    rows = indices_for_oracle(case, idx.cpu().numpy(), toks)
+    ref_out, ref_lse = oracle_attention(case, rows, toks)
+    check_attention(out[toks], lse[toks], ref_out, ref_lse, f"window {win_left + 1}")
+
+
+def test_many_short_sequences():
+    """More sequences than the kernels keep offsets for on chip; many CTAs
+    start and end mid-sequence; hundreds of tokens see one or two keys, so
+    their outputs are single V rows (|out| up to ~4) and any rounding of the
+    largest weight shows directly."""
+    rng = np.random.default_rng(7)
+    lengths = [int(x) for x in rng.integers(1, 40, size=700)]
+    layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=6, index_heads=4, index_dim=64)
+    case = layer_cases(custom_spec(lengths, heads=8, win_left=15, layers=(layer,), seed=3))[0]
+    idx = gpu_topk(case)
+    rows = indices_for_oracle(case, idx.cpu().numpy())
+    out, lse = gpu_attention(case, idx)
+    ref_out, ref_lse = oracle_attention(case, rows)
+    check_attention(out, lse, ref_out, ref_lse, "700 sequences")
