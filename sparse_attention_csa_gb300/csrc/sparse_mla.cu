@@ -169,9 +169,12 @@ __device__ __forceinline__ bool slot_valid(const TokenInfo &ti, const TileDesc &
 // else ceil(nw/128) + ceil(nc/128) (one ring tile when W <= 128). The prefix
 // sums over a sequence are closed forms over the few positions where a
 // ceiling steps. Compressed tiles gathered from a top-k list (positions that
-// see more blocks than top-k keeps) cost a little more than boxed runs.
-constexpr int64_t kTokenCost = 3;
-constexpr int64_t kTileCost = 8;
+// see more blocks than top-k keeps) cost a little more than boxed runs. The
+// three weights are a least-squares fit of measured per-CTA times (GB300,
+// one 152-CTA launch per layer, five layers of 4k-32k-token packs): about 1.7 us a
+// token, 3.8 us a tile and 0.5 us more for a gathered tile.
+constexpr int64_t kTokenCost = 11;
+constexpr int64_t kTileCost = 24;
 constexpr int64_t kGatherCost = 3;  // extra for a compressed tile gathered from a top-k list
 
 struct WorkModel {
