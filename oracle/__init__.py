@@ -38,8 +38,11 @@ def lib():
         _lib.csa_ref_sparse_mla_fwd.argtypes = [
             f64p, f64p, f64p, i32p, i32p, i32p, i32, i32, i32, i32, i32, i32, f64p, C.c_double,
             i32, i32, i32p, i32, f64p, f64p]
+        _lib.csa_ref_sparse_mla_bwd.argtypes = [
+            f64p, f64p, f64p, f64p, i32p, i32p, i32p, i32, i32, i32, i32, i32, i32, f64p,
+            C.c_double, i32, i32, f64p, f64p, f64p, f64p, f64p, f64p]
         for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx",
-                     "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd"):
+                     "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd"):
             getattr(_lib, name).restype = C.c_int
     return _lib
 
@@ -141,3 +144,42 @@ def sparse_mla_fwd(q_rows, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens, cu_se
         _p(sk, C.c_double), float(softmax_scale), cmp_ratio, ori_win_left, _p(tok, C.c_int32), n,
         _p(out, C.c_double), _p(lse, C.c_double)), "sparse_mla_fwd")
     return out, lse
+
+
+def sparse_mla_bwd(q, dout, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens, cu_seqlens_cmp,
+                   sinks, softmax_scale: float, cmp_ratio: int, ori_win_left: int):
+    """Gradients of sum(dout * out) for the whole pack, in fp64, and the
+    head-averaged attention distributions. Returns a dict with d_q [T,H,D],
+    d_ori_kv [T,D], d_cmp_kv [Tc,D] (None without compressed rows), d_sinks
+    [H] (None without sinks), ori_l1 [T,W] and cmp_l1 [T,topk] (None without
+    top-k indices)."""
+    qq = _f64(q)
+    g = _f64(dout)
+    okv = _f64(ori_kv)
+    ckv = _f64(cmp_kv)
+    if ckv is not None and ckv.size == 0:
+        ckv = None
+    idx = _i32(cmp_sparse_indices) if ckv is not None else None
+    topk = 0 if idx is None else idx.shape[1]
+    cu = _i32(cu_seqlens)
+    cuc = _i32(cu_seqlens_cmp)
+    sk = _f64(sinks)
+    t, h, d = qq.shape
+    tc = 0 if ckv is None else ckv.shape[0]
+    w = ori_win_left + 1
+    res = {
+        "d_q": np.zeros((t, h, d)),
+        "d_ori_kv": np.zeros((t, d)),
+        "d_cmp_kv": None if ckv is None else np.zeros((tc, d)),
+        "d_sinks": None if sk is None else np.zeros(h),
+        "ori_l1": np.zeros((t, w)),
+        "cmp_l1": None if idx is None else np.zeros((t, topk)),
+    }
+    _check(lib().csa_ref_sparse_mla_bwd(
+        _p(qq, C.c_double), _p(g, C.c_double), _p(okv, C.c_double), _p(ckv, C.c_double),
+        _p(idx, C.c_int32), _p(cu, C.c_int32), _p(cuc, C.c_int32), len(cu) - 1, t, tc, h, d,
+        topk, _p(sk, C.c_double), float(softmax_scale), cmp_ratio, ori_win_left,
+        _p(res["d_q"], C.c_double), _p(res["d_ori_kv"], C.c_double),
+        _p(res["d_cmp_kv"], C.c_double), _p(res["d_sinks"], C.c_double),
+        _p(res["ori_l1"], C.c_double), _p(res["cmp_l1"], C.c_double)), "sparse_mla_bwd")
+    return res

@@ -12,7 +12,9 @@
  *   - lightning-indexer scores over the causally visible compressed blocks
  *     of the token's own segment, and their top-k;
  *   - shared-KV MLA attention over window rows plus selected compressed
- *     rows, with a per-head attention sink.
+ *     rows, with a per-head attention sink;
+ *   - its backward: gradients of q, of both KV streams and of the sinks,
+ *     and the head-averaged attention distributions.
  * Every floating-point input arrives as double (bf16 inputs are widened
  * exactly by the caller); every sum, exp and log is done in double.
  *
@@ -329,6 +331,169 @@ int csa_ref_sparse_mla_fwd(const double *q, const double *ori_kv, const double *
         }
         free(rows);
         free(logit);
+    }
+    return err;
+}
+
+/*
+ * Backward of the shared-KV MLA attention with sinks (the gradient entry
+ * point the miles PR 2038 report lists as sparse_flash_mla_grad: returns
+ * d_query, d_ori_kv, d_cmp_kv, d_sinks and the head-averaged attention
+ * distributions ori/cmp_softmax_l1_norm, shaped like the window and
+ * compressed index lists).
+ *
+ * The forward is recomputed here in double from q and the KV rows (the
+ * oracle does not trust a caller's out or lse). With l_a = scale q.k_a,
+ * P_a = exp(l_a) / Z, P_sink = exp(sink) / Z and out = sum_a P_a v_a (v = k,
+ * the same row), the loss gradient dout gives, per token t and head h:
+ *   Dv      = dout . out
+ *   dS_a    = P_a (dout . v_a - Dv)
+ *   d_q     = scale sum_a dS_a k_a
+ *   d_row_a += scale dS_a q + P_a dout        (row a as key and as value)
+ *   d_sink  += -P_sink Dv
+ *   l1[slot of a] += P_a / H
+ * d_ori_kv [T, D], d_cmp_kv [Tc, D] and d_sinks [H] are overwritten (zeroed
+ * first); ori_l1 is [n_tokens, W] in window-slot order (slot i <-> row
+ * start + i, zero on the padded tail); cmp_l1 is [n_tokens, topk] in the
+ * order of cmp_sparse_indices (zero where the entry is -1, out of range or
+ * not visible), and is only written when cmp_sparse_indices is given.
+ * Every pointer but q, dout, ori_kv, cu_seqlens, d_q and d_ori_kv may be
+ * NULL where its part is absent or not wanted.
+ */
+int csa_ref_sparse_mla_bwd(const double *q, const double *dout, const double *ori_kv,
+                           const double *cmp_kv, const int32_t *cmp_sparse_indices,
+                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp, int32_t batch,
+                           int32_t T, int32_t Tc, int32_t H, int32_t D, int32_t topk,
+                           const double *sinks, double softmax_scale, int32_t cmp_ratio,
+                           int32_t ori_win_left, double *d_q, double *d_ori_kv, double *d_cmp_kv,
+                           double *d_sinks, double *ori_l1, double *cmp_l1) {
+    if (!q || !dout || !ori_kv || !cu_seqlens || !d_q || !d_ori_kv) return REF_ERR_ARG;
+    if (T < 0 || Tc < 0 || H < 1 || D < 1 || ori_win_left < 0) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, T)) return REF_ERR_ARG;
+    const int use_cmp = cmp_kv != NULL && Tc > 0;
+    if (use_cmp) {
+        if (!cu_seqlens_cmp || cmp_ratio < 1 || !d_cmp_kv) return REF_ERR_ARG;
+        if (!check_cu(cu_seqlens_cmp, batch, Tc)) return REF_ERR_ARG;
+        if (cmp_sparse_indices && topk < 1) return REF_ERR_ARG;
+    }
+    const int32_t W = ori_win_left + 1;
+    const int32_t max_cmp = use_cmp ? (cmp_sparse_indices ? topk : Tc) : 0;
+    memset(d_ori_kv, 0, sizeof(double) * (size_t)T * (size_t)D);
+    if (use_cmp) memset(d_cmp_kv, 0, sizeof(double) * (size_t)Tc * (size_t)D);
+    if (d_sinks) memset(d_sinks, 0, sizeof(double) * (size_t)H);
+    if (ori_l1) memset(ori_l1, 0, sizeof(double) * (size_t)T * (size_t)W);
+    if (cmp_l1 && use_cmp && cmp_sparse_indices)
+        memset(cmp_l1, 0, sizeof(double) * (size_t)T * (size_t)topk);
+    int err = REF_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+        int32_t b = segment_of(cu_seqlens, batch, t);
+        const int32_t n_max = W + max_cmp;
+        const double **rows = (const double **)malloc(sizeof(double *) * (size_t)n_max);
+        double **grads = (double **)malloc(sizeof(double *) * (size_t)n_max);
+        double **l1 = (double **)malloc(sizeof(double *) * (size_t)n_max);
+        double *logit = (double *)malloc(sizeof(double) * (size_t)n_max);
+        double *prob = (double *)malloc(sizeof(double) * (size_t)n_max);
+        double *ds = (double *)malloc(sizeof(double) * (size_t)n_max);
+        double *o = (double *)malloc(sizeof(double) * (size_t)D);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)n_max * (size_t)D);
+        double *sink_acc = (double *)malloc(sizeof(double) * (size_t)H);
+        if (!rows || !grads || !l1 || !logit || !prob || !ds || !o || !acc || !sink_acc) {
+            free(rows), free(grads), free(l1), free(logit), free(prob), free(ds), free(o);
+            free(acc), free(sink_acc);
+            err = REF_ERR_NOMEM;
+            continue;
+        }
+        /* the token's keys, with where their gradient and distribution go */
+        int32_t n = 0;
+        int32_t start = t - W + 1;
+        if (start < cu_seqlens[b]) start = cu_seqlens[b];
+        for (int32_t row = start; row <= t; ++row) {
+            rows[n] = ori_kv + (int64_t)row * D;
+            grads[n] = d_ori_kv + (int64_t)row * D;
+            l1[n] = ori_l1 ? ori_l1 + (int64_t)t * W + (row - start) : NULL;
+            ++n;
+        }
+        if (use_cmp) {
+            if (cmp_sparse_indices) {
+                for (int32_t s = 0; s < topk; ++s) {
+                    int32_t j = cmp_sparse_indices[(int64_t)t * topk + s];
+                    if (j < 0 || j >= Tc) continue;
+                    if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
+                    rows[n] = cmp_kv + (int64_t)j * D;
+                    grads[n] = d_cmp_kv + (int64_t)j * D;
+                    l1[n] = cmp_l1 ? cmp_l1 + (int64_t)t * topk + s : NULL;
+                    ++n;
+                }
+            } else {
+                for (int32_t j = cu_seqlens_cmp[b]; j < cu_seqlens_cmp[b + 1]; ++j) {
+                    if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
+                    rows[n] = cmp_kv + (int64_t)j * D;
+                    grads[n] = d_cmp_kv + (int64_t)j * D;
+                    l1[n] = NULL;
+                    ++n;
+                }
+            }
+        }
+        memset(acc, 0, sizeof(double) * (size_t)n * (size_t)D);
+        for (int32_t h = 0; h < H; ++h) {
+            const double *qh = q + ((int64_t)t * H + h) * D;
+            const double *gh = dout + ((int64_t)t * H + h) * D;
+            double *dqh = d_q + ((int64_t)t * H + h) * D;
+            /* forward again: logits, max, denominator with the sink */
+            double m = -INFINITY;
+            for (int32_t a = 0; a < n; ++a) {
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += qh[d] * rows[a][d];
+                logit[a] = softmax_scale * dot;
+                if (logit[a] > m) m = logit[a];
+            }
+            double sink = sinks ? sinks[h] : -INFINITY;
+            if (sink > m) m = sink;
+            double z = 0.0;
+            for (int32_t a = 0; a < n; ++a) z += exp(logit[a] - m);
+            double p_sink = 0.0;
+            if (sinks && sink != -INFINITY) {
+                z += exp(sink - m);
+                p_sink = exp(sink - m);
+            }
+            p_sink /= z;
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            for (int32_t a = 0; a < n; ++a) {
+                prob[a] = exp(logit[a] - m) / z;
+                for (int32_t d = 0; d < D; ++d) o[d] += prob[a] * rows[a][d];
+            }
+            /* Dv = dout . out; dS_a = P_a (dout . v_a - Dv) */
+            double dv = 0.0;
+            for (int32_t d = 0; d < D; ++d) dv += gh[d] * o[d];
+            for (int32_t a = 0; a < n; ++a) {
+                double dp = 0.0;
+                for (int32_t d = 0; d < D; ++d) dp += gh[d] * rows[a][d];
+                ds[a] = prob[a] * (dp - dv);
+            }
+            for (int32_t d = 0; d < D; ++d) {
+                double s = 0.0;
+                for (int32_t a = 0; a < n; ++a) s += ds[a] * rows[a][d];
+                dqh[d] = softmax_scale * s;
+            }
+            for (int32_t a = 0; a < n; ++a) {
+                double *ga = acc + (int64_t)a * D;
+                for (int32_t d = 0; d < D; ++d)
+                    ga[d] += softmax_scale * ds[a] * qh[d] + prob[a] * gh[d];
+                if (l1[a]) *l1[a] += prob[a] / H;
+            }
+            sink_acc[h] = -p_sink * dv;
+        }
+        /* the rows are shared between tokens: add this token's part in turn */
+#pragma omp critical(csa_ref_bwd_scatter)
+        {
+            for (int32_t a = 0; a < n; ++a)
+                for (int32_t d = 0; d < D; ++d) grads[a][d] += acc[(int64_t)a * D + d];
+            if (d_sinks)
+                for (int32_t h = 0; h < H; ++h) d_sinks[h] += sink_acc[h];
+        }
+        free(rows), free(grads), free(l1), free(logit), free(prob), free(ds), free(o);
+        free(acc), free(sink_acc);
     }
     return err;
 }

@@ -73,11 +73,13 @@ def topk_dense(scores, visible, k):
     return out
 
 
-def attention_dense(q, ori_kv, cmp_kv, lengths, W, r, selected, sinks, scale):
+def attention_dense(q, ori_kv, cmp_kv, lengths, W, r, selected, sinks, scale, return_probs=False):
     """Dense masked attention with a sink column.
 
     ``selected`` is a [T, Tc] bool mask of the compressed rows each token
-    attends (may be None when there are no compressed rows)."""
+    attends (may be None when there are no compressed rows). With
+    ``return_probs`` the attention weights come back too, [T, H, T + Tc + 1]:
+    original rows, then compressed rows, then the sink column."""
     T, H, D = q.shape
     kv = ori_kv if cmp_kv is None else np.concatenate([ori_kv, cmp_kv], axis=0)
     mask = window_mask(lengths, W)
@@ -94,4 +96,6 @@ def attention_dense(q, ori_kv, cmp_kv, lengths, W, r, selected, sinks, scale):
     p = e / z
     out = np.einsum("thk,kd->thd", p[:, :, :-1], kv)
     lse = (mx + np.log(z))[:, :, 0]
+    if return_probs:
+        return out, lse, p
     return out, lse
