@@ -184,6 +184,49 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
                                 int32_t return_softmax_lse, csa_stream_t stream);
 
 /*
+ * Backward of csa_sparse_mla_fwd.
+ * [miles#2038] report and [hp#RFC] section 4 (npu_sparse_flash_mla_grad:
+ * from q, dout, the forward's attn_out and softmax_lse it returns d_query,
+ * d_ori_kv, d_cmp_kv, d_sinks, and ori/cmp_softmax_l1_norm, the attention
+ * distribution averaged over heads, shaped like the window and compressed
+ * index lists). Keys, masks, sinks and scale exactly as csa_sparse_mla_fwd;
+ * with P_a = exp(softmax_scale q.kv_a - lse), P_sink = exp(sink - lse) and
+ * Dv = dout . out, per token t and head h:
+ *     dS_a  = P_a (dout[t,h,:] . kv_a - Dv)
+ *     d_q[t,h,:]      = softmax_scale sum_a dS_a kv_a
+ *     d_row(kv_a)    += softmax_scale dS_a q[t,h,:] + P_a dout[t,h,:]
+ *     d_sinks[h]     -= P_sink Dv
+ *     l1[t, slot(a)] += P_a / H
+ * (the row's gradient counts it both as key and as value: it is one row).
+ * Inputs: q, dout, out [T, H, D] bf16 (out and softmax_lse [T, H] fp32 are
+ * what csa_sparse_mla_fwd returned for the same arguments); the rest as
+ * csa_sparse_mla_fwd. Outputs, all fp32 and overwritten:
+ *   d_q [T, H, D];  d_ori_kv [T, D];  d_cmp_kv [Tc, D] (when cmp_kv is used);
+ *   d_sinks [H] (when sinks is given; may be NULL to skip);
+ *   ori_softmax_l1_norm [T, ori_win_left + 1] or NULL: slot i is window row
+ *     max(t - ori_win_left, segment start) + i, zero past the token itself;
+ *   cmp_softmax_l1_norm [T, topk] or NULL: slot i follows
+ *     cmp_sparse_indices[t, i], zero where that entry is skipped; only with
+ *     cmp_sparse_indices (with every visible row there is no list).
+ * The KV-row gradients are sums over tokens made with fp32 atomics, so their
+ * last bits depend on the order the tokens finish in.
+ * Errors: as csa_sparse_mla_fwd, plus NULL dout/out/softmax_lse/d_q/d_ori_kv
+ * (or d_cmp_kv when cmp_kv is used) -> CSA_ERR_NULL. q, dout, out, ori_kv,
+ * cmp_kv must be 4-byte aligned.
+ */
+csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, const csa_bf16_t *out,
+                                const float *softmax_lse, const csa_bf16_t *ori_kv,
+                                const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_ori_kv,
+                                const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                int32_t total_tokens, int32_t total_cmp, int32_t heads,
+                                int32_t head_dim, int32_t topk, const float *sinks,
+                                float softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
+                                int32_t ori_win_right, float *d_q, float *d_ori_kv,
+                                float *d_cmp_kv, float *d_sinks, float *ori_softmax_l1_norm,
+                                float *cmp_softmax_l1_norm, csa_stream_t stream);
+
+/*
  * csa_indexer_topk without a workspace, for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point.
  *

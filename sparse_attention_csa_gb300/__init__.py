@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) forward path of DeepSeek-V4 Compressed Sparse Attention.
+"""GB300 (sm_103a) forward path of DeepSeek-V4 Compressed Sparse Attention,
+and the backward of its sparse MLA attention.
 
 Thin Python binding of the C ABI declared in ``include/csa.h`` (same call
 names). It only marshals arguments: every step of the path runs in the CUDA
@@ -20,7 +21,8 @@ import torch
 __all__ = [
     "CsaError", "lib", "library_path", "csa_status_string", "csa_compress_cu_seqlens",
     "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
-    "csa_sparse_mla_fwd", "csa_device_error", "csa_indexer_topk_noalloc", "EXPORTED_SYMBOLS",
+    "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +32,7 @@ library_path = os.path.join(_HERE, "_build", "libcsa_gb300.so")
 EXPORTED_SYMBOLS = (
     "csa_status_string", "csa_compress_cu_seqlens", "csa_window_idx",
     "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
-    "csa_device_error", "csa_indexer_topk_noalloc",
+    "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -68,11 +70,15 @@ def lib():
         L.csa_sparse_mla_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                          _i32, _i32, _vp, _f32, _i32, _i32, _i32, _vp, _vp, _i32,
                                          _vp]
+        L.csa_sparse_mla_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                         _i32, _i32, _i32, _i32, _i32, _vp, _f32, _i32, _i32,
+                                         _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.csa_device_error.argtypes = [_vp, C.POINTER(_i32)]
         L.csa_indexer_topk_noalloc.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp,
                                                _i32, _i32, _i32, _vp, _vp, _vp]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
-                     "csa_sparse_mla_fwd", "csa_device_error", "csa_indexer_topk_noalloc"):
+                     "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error",
+                     "csa_indexer_topk_noalloc"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -233,6 +239,48 @@ def csa_sparse_mla_fwd(q, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens_q, cu_s
         _ptr(lse) if return_softmax_lse else None, 1 if return_softmax_lse else 0,
         _stream(stream)), "csa_sparse_mla_fwd")
     return out, (lse if return_softmax_lse else None)
+
+
+def csa_sparse_mla_bwd(q, dout, out, lse, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens_q,
+                       cu_seqlens_ori_kv, cu_seqlens_cmp_kv, sinks, softmax_scale: float,
+                       cmp_ratio: int, ori_win_left: int, ori_win_right: int = 0,
+                       want_l1: bool = True, stream=None):
+    """Backward of ``csa_sparse_mla_fwd`` from its ``out`` and ``lse``.
+
+    Returns a dict of fp32 tensors: d_q [T,H,D], d_ori_kv [T,D], d_cmp_kv
+    [Tc,D] (None without compressed rows), d_sinks [H] (None without sinks),
+    ori_l1 [T, ori_win_left+1] and cmp_l1 [T, topk] (None without a top-k
+    list, or both None when ``want_l1`` is false)."""
+    for t, n, dt, nd in ((q, "q", torch.bfloat16, 3), (dout, "dout", torch.bfloat16, 3),
+                         (out, "out", torch.bfloat16, 3), (lse, "lse", torch.float32, 2),
+                         (ori_kv, "ori_kv", torch.bfloat16, 2), (cmp_kv, "cmp_kv", torch.bfloat16, 2),
+                         (cmp_sparse_indices, "cmp_sparse_indices", torch.int32, 2),
+                         (cu_seqlens_q, "cu_seqlens_q", torch.int32, 1),
+                         (cu_seqlens_ori_kv, "cu_seqlens_ori_kv", torch.int32, 1),
+                         (cu_seqlens_cmp_kv, "cu_seqlens_cmp_kv", torch.int32, 1),
+                         (sinks, "sinks", torch.float32, 1)):
+        _need(t, n, dt, nd)
+    T, H, D = q.shape
+    Tc = 0 if cmp_kv is None else cmp_kv.shape[0]
+    topk = 0 if cmp_sparse_indices is None else cmp_sparse_indices.shape[1]
+    f32 = dict(dtype=torch.float32, device=q.device)
+    res = {
+        "d_q": torch.empty((T, H, D), **f32),
+        "d_ori_kv": torch.empty((T, D), **f32),
+        "d_cmp_kv": torch.empty((Tc, D), **f32) if Tc else None,
+        "d_sinks": torch.empty((H,), **f32) if sinks is not None else None,
+        "ori_l1": torch.empty((T, ori_win_left + 1), **f32) if want_l1 else None,
+        "cmp_l1": (torch.empty((T, topk), **f32)
+                   if want_l1 and Tc and cmp_sparse_indices is not None else None),
+    }
+    _check(lib().csa_sparse_mla_bwd(
+        _ptr(q), _ptr(dout), _ptr(out), _ptr(lse), _ptr(ori_kv), _ptr(cmp_kv) if Tc else None,
+        _ptr(cmp_sparse_indices), _ptr(cu_seqlens_q), _ptr(cu_seqlens_ori_kv),
+        _ptr(cu_seqlens_cmp_kv), cu_seqlens_q.numel() - 1, T, Tc, H, D, topk, _ptr(sinks),
+        float(softmax_scale), int(cmp_ratio), int(ori_win_left), int(ori_win_right),
+        _ptr(res["d_q"]), _ptr(res["d_ori_kv"]), _ptr(res["d_cmp_kv"]), _ptr(res["d_sinks"]),
+        _ptr(res["ori_l1"]), _ptr(res["cmp_l1"]), _stream(stream)), "csa_sparse_mla_bwd")
+    return res
 
 
 def csa_device_error(stream=None):

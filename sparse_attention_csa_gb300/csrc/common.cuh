@@ -21,6 +21,7 @@ enum KernelId : int32_t {
     kKerWindow = 2,
     kKerIndexer = 3,
     kKerMla = 4,
+    kKerMlaBwd = 5,
 };
 
 __device__ __forceinline__ void report_error(int32_t *err, int32_t kind, int32_t kernel,

@@ -134,6 +134,68 @@ csa_status_t csa_indexer_topk(const csa_bf16_t *q, const csa_bf16_t *k, const fl
     return from_cuda(csa::launch_indexer_topk(a, (cudaStream_t)stream));
 }
 
+csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, const csa_bf16_t *out,
+                                const float *softmax_lse, const csa_bf16_t *ori_kv,
+                                const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
+                                const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_ori_kv,
+                                const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                int32_t total_tokens, int32_t total_cmp, int32_t heads,
+                                int32_t head_dim, int32_t topk, const float *sinks,
+                                float softmax_scale, int32_t cmp_ratio, int32_t ori_win_left,
+                                int32_t ori_win_right, float *d_q, float *d_ori_kv,
+                                float *d_cmp_kv, float *d_sinks, float *ori_softmax_l1_norm,
+                                float *cmp_softmax_l1_norm, csa_stream_t stream) {
+    const bool use_cmp = cmp_kv != nullptr && total_cmp > 0;
+    if (batch < 0 || total_tokens < 0 || total_cmp < 0 || heads < 1 || ori_win_left < 0)
+        return CSA_ERR_SHAPE;
+    if (total_tokens > 0) {  // empty buffers may be NULL
+        if (!q || !dout || !out || !softmax_lse || !ori_kv || !cu_seqlens_q || !d_q || !d_ori_kv)
+            return CSA_ERR_NULL;
+        if (use_cmp && (!cu_seqlens_cmp_kv || !d_cmp_kv)) return CSA_ERR_NULL;
+    }
+    if (use_cmp && cmp_sparse_indices && topk < 1) return CSA_ERR_SHAPE;
+    if (head_dim != 512) return CSA_ERR_UNSUPPORTED;
+    if (heads > 64) return CSA_ERR_UNSUPPORTED;
+    if (ori_win_right != 0 || ori_win_left > 1023) return CSA_ERR_UNSUPPORTED;
+    if (use_cmp && cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    if (use_cmp && cmp_sparse_indices && topk > 1024) return CSA_ERR_UNSUPPORTED;
+    if (cu_seqlens_ori_kv && cu_seqlens_ori_kv != cu_seqlens_q) return CSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)q & 3u) || ((uintptr_t)dout & 3u) || ((uintptr_t)out & 3u) ||
+        ((uintptr_t)ori_kv & 3u) || (use_cmp && ((uintptr_t)cmp_kv & 3u)))
+        return CSA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return CSA_OK;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    csa::MlaBwdArgs a;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.dout = reinterpret_cast<const __nv_bfloat16 *>(dout);
+    a.out = reinterpret_cast<const __nv_bfloat16 *>(out);
+    a.lse = softmax_lse;
+    a.ori_kv = reinterpret_cast<const __nv_bfloat16 *>(ori_kv);
+    a.cmp_kv = use_cmp ? reinterpret_cast<const __nv_bfloat16 *>(cmp_kv) : nullptr;
+    a.cmp_idx = use_cmp ? cmp_sparse_indices : nullptr;
+    a.cu_q = cu_seqlens_q;
+    a.cu_c = use_cmp ? cu_seqlens_cmp_kv : nullptr;
+    a.sinks = sinks;
+    a.d_q = d_q;
+    a.d_ori_kv = d_ori_kv;
+    a.d_cmp_kv = use_cmp ? d_cmp_kv : nullptr;
+    a.d_sinks = sinks ? d_sinks : nullptr;
+    a.ori_l1 = ori_softmax_l1_norm;
+    a.cmp_l1 = use_cmp && cmp_sparse_indices ? cmp_softmax_l1_norm : nullptr;
+    a.err = err;
+    a.T = total_tokens;
+    a.Tc = use_cmp ? total_cmp : 0;
+    a.H = heads;
+    a.batch = batch;
+    a.topk = use_cmp && cmp_sparse_indices ? topk : 0;
+    a.cmp_ratio = use_cmp ? cmp_ratio : 1;
+    a.window = ori_win_left + 1;
+    a.softmax_scale = softmax_scale;
+    return from_cuda(csa::launch_sparse_mla_bwd(a, (cudaStream_t)stream));
+}
+
 csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
                                 const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_ori_kv,

@@ -54,6 +54,30 @@ struct MlaArgs {
 };
 
 cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);
+
+struct MlaBwdArgs {
+    const __nv_bfloat16 *q;       // [T, H, 512]
+    const __nv_bfloat16 *dout;    // [T, H, 512]
+    const __nv_bfloat16 *out;     // [T, H, 512], the forward's output
+    const float *lse;             // [T, H], the forward's log-sum-exp
+    const __nv_bfloat16 *ori_kv;  // [T, 512]
+    const __nv_bfloat16 *cmp_kv;  // [Tc, 512] or nullptr
+    const int32_t *cmp_idx;       // [T, topk] or nullptr (all visible)
+    const int32_t *cu_q;          // [batch+1]
+    const int32_t *cu_c;          // [batch+1] (required when cmp_kv is used)
+    const float *sinks;           // [H] or nullptr
+    float *d_q;                   // [T, H, 512]
+    float *d_ori_kv;              // [T, 512]
+    float *d_cmp_kv;              // [Tc, 512] (when cmp_kv is used)
+    float *d_sinks;               // [H] or nullptr
+    float *ori_l1;                // [T, window] or nullptr
+    float *cmp_l1;                // [T, topk] or nullptr
+    int32_t *err;
+    int32_t T, Tc, H, batch, topk, cmp_ratio, window;
+    float softmax_scale;
+};
+
+cudaError_t launch_sparse_mla_bwd(const MlaBwdArgs &a, cudaStream_t stream);
 // Largest topk (entries of cmp_sparse_indices per token) the kernel accepts.
 int32_t sparse_mla_max_topk();
 
