@@ -66,6 +66,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--bwd", action="store_true",
+                   help="also time the sparse MLA backward of every layer and print its own "
+                        "JSON line after the forward's (off by default: one line per run)")
+    p.add_argument("--bwd-steps", type=int, default=5)
     return p.parse_args()
 
 
@@ -458,7 +462,65 @@ def run_ours(args, world, rank, local):
         result["e2e"] = run_e2e(args, layers, stream, flush, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(layers, args.cpu_seconds)
+    if args.bwd and rank == 0:
+        result["_bwd"] = run_bwd(args, layers, stream, flush, peaks, peak_kind)
     return result
+
+
+def run_bwd(args, layers, stream, flush, peaks, peak_src):
+    """The sparse MLA backward of each layer (from that layer's forward out and
+    lse, seeded N(0,1) dout), timed per launch with CUDA events between L2
+    flushes. Algorithmic FLOPs per (key, head): 2D each for the recomputed
+    scores, dout . k, d_q and the row gradient's two terms -> 10 D."""
+    import sparse_attention_csa_gb300 as csa
+    gen = torch.Generator().manual_seed(7)
+    per, flops = {}, 0
+    for L in layers:
+        spec, r = L.spec, L.layer.cmp_ratio
+        dout = torch.randn(tuple(L.out.shape), generator=gen).to(torch.bfloat16).to(L.out.device)
+        L.launches(stream)  # this layer's out, lse and top-k rows
+        idx = L.idx if L.layer.indexer else None
+
+        def call():
+            return csa.csa_sparse_mla_bwd(L.dev["q"], dout, L.out, L.lse, L.dev["ori_kv"],
+                                          L.dev["cmp_kv"], idx, L.dev["cu"], L.dev["cu"], L.cuc,
+                                          L.dev["sinks"], spec.scale, r, spec.win_left,
+                                          stream=stream)
+
+        for _ in range(2):
+            flush.zero_()
+            call()
+        ms = []
+        for _ in range(args.bwd_steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        per[f"sparse_mla_bwd/r{r}"] = statistics.median(ms)
+        flops += 10 * spec.dim * spec.heads * L.acc["keys"]
+    st, word = csa.csa_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the backward: {word:#x}")
+    total = sum(per.values())
+    spec = layers[0].spec
+    achieved = flops / (total * 1e-3) / 1e12
+    return {
+        "metric": "sparse MLA backward tokens/s (d_q, d_kv, d_sinks, distributions) on 1 GB300",
+        "value": spec.total_tokens / (total * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.bwd_steps, "warmup": 2, "ms_per_step": total, "higher_is_better": True,
+        "dtype": "fp32 (CUDA cores) from bf16", "data": "synthetic", "part": "backward",
+        "config": {"workload": f"{spec.name}, every layer, forward out/lse as inputs",
+                   "l2": "flushed between launches"},
+        "kernels_ms": per,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": peak_src, "flops": flops,
+                     "note": "first version runs on the CUDA cores; the bound is the bf16 "
+                             "tensor peak the backward's contractions belong on"},
+    }
 
 
 def run_e2e(args, layers, stream, flush, world, device):
@@ -565,8 +627,11 @@ def main():
         return
     world, rank, local = dist_setup("nccl")
     res = run_ours(args, world, rank, local)
+    bwd = res.pop("_bwd", None)
     if rank == 0:
         print(json.dumps(res), flush=True)
+        if bwd is not None:
+            print(json.dumps(bwd), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
