@@ -117,6 +117,34 @@ def test_mla_rejects(L):
     assert call(q=C.c_void_p(0x1002)) == 3  # 16-byte alignment
 
 
+def test_mla_bwd_rejects(L):
+    names = ["q", "dout", "out", "lse", "okv", "ckv", "idx", "cuq", "cuo", "cuc", "batch", "T",
+             "Tc", "H", "D", "topk", "sinks", "scale", "r", "wl", "wr", "dq", "dokv", "dckv",
+             "dsinks", "ol1", "cl1", "stream"]
+    base = dict(q=P, dout=P, out=P, lse=P, okv=P, ckv=P, idx=P, cuq=P, cuo=NUL, cuc=P, batch=3,
+                T=256, Tc=63, H=4, D=512, topk=8, sinks=P, scale=C.c_float(0.044), r=4, wl=15,
+                wr=0, dq=P, dokv=P, dckv=P, dsinks=P, ol1=P, cl1=P, stream=NUL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.csa_sparse_mla_bwd(*[a[n] for n in names])
+
+    for k in ("q", "dout", "out", "lse", "okv", "cuq", "dq", "dokv", "cuc", "dckv"):
+        assert call(**{k: NUL}) == 1, k
+    assert call(H=0) == 2
+    assert call(T=-3) == 2
+    assert call(topk=0) == 2
+    assert call(D=576) == 3
+    assert call(H=65) == 3
+    assert call(wr=1) == 3
+    assert call(wl=1024) == 3
+    assert call(r=1) == 3
+    assert call(cuo=C.c_void_p(0x2000)) == 3  # prefix-KV cu_seqlens
+    assert call(topk=1025) == 3
+    assert call(dout=C.c_void_p(0x1001)) == 3  # 4-byte alignment
+
+
 def test_product_does_not_import_oracle():
     pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
     for dirpath, _, files in os.walk(pkg):
