@@ -511,15 +511,13 @@ def run_bwd(args, layers, stream, flush, peaks, peak_src):
         "metric": "sparse MLA backward tokens/s (d_q, d_kv, d_sinks, distributions) on 1 GB300",
         "value": spec.total_tokens / (total * 1e-3), "unit": UNIT, "n_gpus": 1,
         "steps": args.bwd_steps, "warmup": 2, "ms_per_step": total, "higher_is_better": True,
-        "dtype": "fp32 (CUDA cores) from bf16", "data": "synthetic", "part": "backward",
+        "dtype": "bf16 (tcgen05, fp32 accumulate)", "data": "synthetic", "part": "backward",
         "config": {"workload": f"{spec.name}, every layer, forward out/lse as inputs",
                    "l2": "flushed between launches"},
         "kernels_ms": per,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "peak_source": peak_src, "flops": flops,
-                     "note": "first version runs on the CUDA cores; the bound is the bf16 "
-                             "tensor peak the backward's contractions belong on"},
+                     "peak_source": peak_src, "flops": flops},
     }
 
 

@@ -211,8 +211,9 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
  * The KV-row gradients are sums over tokens made with fp32 atomics, so their
  * last bits depend on the order the tokens finish in.
  * Errors: as csa_sparse_mla_fwd, plus NULL dout/out/softmax_lse/d_q/d_ori_kv
- * (or d_cmp_kv when cmp_kv is used) -> CSA_ERR_NULL. q, dout, out, ori_kv,
- * cmp_kv must be 4-byte aligned.
+ * (or d_cmp_kv when cmp_kv is used) -> CSA_ERR_NULL. q, dout, ori_kv,
+ * cmp_kv, d_ori_kv and d_cmp_kv must be 16-byte aligned, out 4-byte aligned
+ * (else CSA_ERR_UNSUPPORTED).
  */
 csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, const csa_bf16_t *out,
                                 const float *softmax_lse, const csa_bf16_t *ori_kv,

@@ -160,9 +160,11 @@ csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, con
     if (use_cmp && cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
     if (use_cmp && cmp_sparse_indices && topk > 1024) return CSA_ERR_UNSUPPORTED;
     if (cu_seqlens_ori_kv && cu_seqlens_ori_kv != cu_seqlens_q) return CSA_ERR_UNSUPPORTED;
-    if (((uintptr_t)q & 3u) || ((uintptr_t)dout & 3u) || ((uintptr_t)out & 3u) ||
-        ((uintptr_t)ori_kv & 3u) || (use_cmp && ((uintptr_t)cmp_kv & 3u)))
+    if (((uintptr_t)q & 15u) || ((uintptr_t)dout & 15u) || ((uintptr_t)out & 3u) ||
+        ((uintptr_t)ori_kv & 15u) || (use_cmp && ((uintptr_t)cmp_kv & 15u)))
         return CSA_ERR_UNSUPPORTED;
+    if (((uintptr_t)d_ori_kv & 15u) || (use_cmp && ((uintptr_t)d_cmp_kv & 15u)))
+        return CSA_ERR_UNSUPPORTED;  // the row gradients are added 16 bytes at a time
     if (total_tokens == 0) return CSA_OK;
     csa_status_t st;
     int32_t *err = error_word(&st);

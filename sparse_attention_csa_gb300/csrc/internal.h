@@ -78,6 +78,8 @@ struct MlaBwdArgs {
 };
 
 cudaError_t launch_sparse_mla_bwd(const MlaBwdArgs &a, cudaStream_t stream);
+// The tensor-core kernel alone (outputs already zeroed where they accumulate).
+cudaError_t launch_sparse_mla_bwd_tc(const MlaBwdArgs &a, cudaStream_t stream);
 // Largest topk (entries of cmp_sparse_indices per token) the kernel accepts.
 int32_t sparse_mla_max_topk();
 

@@ -142,7 +142,8 @@ def test_mla_bwd_rejects(L):
     assert call(r=1) == 3
     assert call(cuo=C.c_void_p(0x2000)) == 3  # prefix-KV cu_seqlens
     assert call(topk=1025) == 3
-    assert call(dout=C.c_void_p(0x1001)) == 3  # 4-byte alignment
+    assert call(dout=C.c_void_p(0x1008)) == 3  # 16-byte alignment
+    assert call(dokv=C.c_void_p(0x1004)) == 3
 
 
 def test_product_does_not_import_oracle():
