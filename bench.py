@@ -24,7 +24,9 @@ Extra objects on the JSON line:
 * clocks    -- nvidia-smi samples taken during the timed region.
 
 ``--impl reference`` times the oracle itself as the step (a bounded token
-sample per step) on the host cores.
+sample per step) on the host cores. ``--bwd`` adds a second JSON line: the
+sparse MLA backward of every layer, timed per launch from the forward's out
+and lse, with its FLOPs against the bf16 tensor peak.
 """
 
 from __future__ import annotations

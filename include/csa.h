@@ -1,7 +1,8 @@
 /*
  * csa.h -- C ABI of the GB300 (sm_103a) forward path of DeepSeek-V4
  * Compressed Sparse Attention (CSA) and its compressor-only mode (HCA) over
- * THD-packed variable-length sequences, on one GPU.
+ * THD-packed variable-length sequences, on one GPU, and of the backward of
+ * its sparse MLA attention.
  *
  * Sources (web pages, cited by title and section):
  *   [miles#2038]  "PR #2038 完整报告" (radixark/miles): "Enable THD
@@ -10,7 +11,8 @@
  *                 (key source excerpts: thd_utils.py, compressor.py), 风险与影响.
  *   [hp#RFC]      "【RFC】DeepSeek-V4 CSA/HCA 自定义算子接入与对外接口对标
  *                 torch_extension" (hyper-parallel); sections 背景 (background),
- *                 1 npu_lightning_indexer, 2 npu_sparse_flash_mla, 缺失入参的用途分析
+ *                 1 npu_lightning_indexer, 2 npu_sparse_flash_mla,
+ *                 4 npu_sparse_flash_mla_grad, 缺失入参的用途分析
  *                 (analysis of the missing arguments).
  *   [MS#4842]     MindSpeed-LLM PR 4842; section 主要改动 (main changes):
  *                 LayerCompressMode {NO_COMPRESS, COMPRESSOR_ONLY, INDEXER}.
