@@ -41,8 +41,12 @@ def lib():
         _lib.csa_ref_sparse_mla_bwd.argtypes = [
             f64p, f64p, f64p, f64p, i32p, i32p, i32p, i32, i32, i32, i32, i32, i32, f64p,
             C.c_double, i32, i32, f64p, f64p, f64p, f64p, f64p, f64p]
+        _lib.csa_ref_indexer_kl_loss_grad.argtypes = [
+            f64p, f64p, f64p, i32p, f64p, i32, i32, i32, i32, i32, i32p, i32p, i32, i32,
+            C.c_double, i32p, i32, f64p, f64p, f64p, f64p]
         for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx",
-                     "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd"):
+                     "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd",
+                     "csa_ref_indexer_kl_loss_grad"):
             getattr(_lib, name).restype = C.c_int
     return _lib
 
@@ -182,4 +186,35 @@ def sparse_mla_bwd(q, dout, ori_kv, cmp_kv, cmp_sparse_indices, cu_seqlens, cu_s
         _p(res["d_q"], C.c_double), _p(res["d_ori_kv"], C.c_double),
         _p(res["d_cmp_kv"], C.c_double), _p(res["d_sinks"], C.c_double),
         _p(res["ori_l1"], C.c_double), _p(res["cmp_l1"], C.c_double)), "sparse_mla_bwd")
+    return res
+
+
+def indexer_kl_loss_grad(q_rows, k, w_rows, sparse_indices, attn_l1, total_tokens: int,
+                         cu_seqlens, cu_seqlens_cmp, cmp_ratio: int, grad_scale: float = 1.0,
+                         tokens=None, want_dk: bool = True):
+    """KL loss of the indexer against the attention distribution, and its
+    gradients, in fp64. ``q_rows``, ``w_rows``, ``sparse_indices`` and
+    ``attn_l1`` hold one row per listed token (all tokens when ``tokens`` is
+    None). Returns a dict: loss [n], d_q [n,Hi,Di], d_w [n,Hi] and d_k [Tc,Di]
+    (the listed tokens' contributions; None unless ``want_dk``)."""
+    q = _f64(q_rows)
+    w = _f64(w_rows)
+    kk = _f64(k)
+    a = _f64(attn_l1)
+    idx = _i32(sparse_indices)
+    cu, cuc = _i32(cu_seqlens), _i32(cu_seqlens_cmp)
+    tok = _i32(tokens)
+    n, hi, di = q.shape
+    topk = idx.shape[1]
+    tc = 0 if kk is None else kk.shape[0]
+    if kk is not None and kk.size == 0:
+        kk = None
+    res = {"loss": np.zeros(n), "d_q": np.zeros((n, hi, di)), "d_w": np.zeros((n, hi)),
+           "d_k": np.zeros((tc, di)) if want_dk else None}
+    _check(lib().csa_ref_indexer_kl_loss_grad(
+        _p(q, C.c_double), _p(kk, C.c_double), _p(w, C.c_double), _p(idx, C.c_int32),
+        _p(a, C.c_double), total_tokens, tc, hi, di, topk, _p(cu, C.c_int32),
+        _p(cuc, C.c_int32), len(cu) - 1, cmp_ratio, float(grad_scale), _p(tok, C.c_int32), n,
+        _p(res["d_q"], C.c_double), _p(res["d_k"], C.c_double), _p(res["d_w"], C.c_double),
+        _p(res["loss"], C.c_double)), "indexer_kl_loss_grad")
     return res

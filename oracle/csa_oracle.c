@@ -14,7 +14,8 @@
  *   - shared-KV MLA attention over window rows plus selected compressed
  *     rows, with a per-head attention sink;
  *   - its backward: gradients of q, of both KV streams and of the sinks,
- *     and the head-averaged attention distributions.
+ *     and the head-averaged attention distributions;
+ *   - the indexer's KL loss against that distribution, and its gradients.
  * Every floating-point input arrives as double (bf16 inputs are widened
  * exactly by the caller); every sum, exp and log is done in double.
  *
@@ -494,6 +495,145 @@ int csa_ref_sparse_mla_bwd(const double *q, const double *dout, const double *or
         }
         free(rows), free(grads), free(l1), free(logit), free(prob), free(ds), free(o);
         free(acc), free(sink_acc);
+    }
+    return err;
+}
+
+/*
+ * Indexer KL-loss gradient (the hyper-parallel RFC, section 3,
+ * sparse_lightning_indexer_kl_loss_grad(q, k, w, sparse_indices,
+ * attn_softmax_l1_norm, cu_seqlens_q, cu_seqlens_k, mask_mode=3, cmp_ratio):
+ * "indexer backward + KL loss", fed with the main attention's target
+ * distribution p that sparse_flash_mla_grad returns as softmax_l1_norm;
+ * MindSpeed-LLM PR 4842, main changes: under TND the loss is normalised by
+ * the global token count, passed as a gradient scale).
+ *
+ * Reading (the pages print the argument list, not the loss): for token t,
+ * the entries s of sparse_indices[t] that name a row j in [0, Tc) visible to
+ * t (the same causal rule as the indexer, mask_mode 3) form its set S.
+ *     I_s  = sum_h w[t,h] * max(0, q[t,h,:] . k[j_s,:])   (indexer score)
+ *     p_s  = a_s / sum_{u in S} a_u,   a = attn_softmax_l1_norm[t, :]
+ *     pi_s = exp(I_s) / sum_{u in S} exp(I_u)
+ *     loss[t] = sum_{s in S, p_s > 0} p_s (log p_s - log pi_s)
+ * i.e. KL(p || softmax(I)) over the selected rows, with p the attention
+ * distribution L1-normalised over the same rows. A token with no entry in S,
+ * or whose entries in S carry no mass, has loss 0 and no gradient.
+ * Gradients of L = grad_scale * sum_t loss[t] (p is a target, not
+ * differentiated), with g_s = grad_scale (pi_s - p_s) = dL/dI_s:
+ *     d_w[t,h]    = sum_s g_s max(0, a_hs)
+ *     d_q[t,h,:]  = sum_s g_s w[t,h] [a_hs > 0] k[j_s,:]
+ *     d_k[j_s,:] += g_s sum_h w[t,h] [a_hs > 0] q[t,h,:]
+ * with a_hs = q[t,h,:] . k[j_s,:] and the ReLU's derivative 0 at 0.
+ * Each entry counts on its own (a row listed twice contributes twice).
+ *
+ * Rows of q, w, sparse_indices, attn_l1, d_q, d_w and loss are per listed
+ * token (tokens == NULL: all T tokens, row i is token i); d_k [Tc, Di] is
+ * overwritten with the contributions of the listed tokens (may be NULL).
+ */
+int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double *w,
+                                 const int32_t *sparse_indices, const double *attn_l1, int32_t T,
+                                 int32_t Tc, int32_t Hi, int32_t Di, int32_t topk,
+                                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp,
+                                 int32_t batch, int32_t cmp_ratio, double grad_scale,
+                                 const int32_t *tokens, int32_t n_tokens, double *d_q, double *d_k,
+                                 double *d_w, double *loss) {
+    if (!q || !w || !sparse_indices || !attn_l1 || !cu_seqlens || !cu_seqlens_cmp) return REF_ERR_ARG;
+    if (!d_q || !d_w || !loss) return REF_ERR_ARG;
+    if (Tc > 0 && !k) return REF_ERR_ARG;
+    if (T < 0 || Tc < 0 || Hi < 1 || Di < 1 || topk < 1 || cmp_ratio < 1 || n_tokens < 0) return REF_ERR_ARG;
+    if (!tokens && n_tokens != T) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, T)) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens_cmp, batch, Tc)) return REF_ERR_ARG;
+    if (d_k) memset(d_k, 0, sizeof(double) * (size_t)Tc * (size_t)Di);
+    int err = REF_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        int32_t t = tokens ? tokens[i] : i;
+        double *dq = d_q + (int64_t)i * Hi * Di;
+        double *dw = d_w + (int64_t)i * Hi;
+        for (int64_t e = 0; e < (int64_t)Hi * Di; ++e) dq[e] = 0.0;
+        for (int32_t h = 0; h < Hi; ++h) dw[h] = 0.0;
+        loss[i] = 0.0;
+        if (t < 0 || t >= T) {
+            err = REF_ERR_ARG;
+            continue;
+        }
+        int32_t b = segment_of(cu_seqlens, batch, t);
+        int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk);
+        double *score = (double *)malloc(sizeof(double) * (size_t)topk);
+        double *p = (double *)malloc(sizeof(double) * (size_t)topk);
+        double *dots = (double *)malloc(sizeof(double) * (size_t)topk * (size_t)Hi);
+        double *gk = (double *)malloc(sizeof(double) * (size_t)topk * (size_t)Di);
+        if (!rows || !score || !p || !dots || !gk) {
+            free(rows), free(score), free(p), free(dots), free(gk);
+            err = REF_ERR_NOMEM;
+            continue;
+        }
+        /* the token's set S, its scores and its target mass */
+        int32_t n = 0;
+        double mass = 0.0;
+        for (int32_t s = 0; s < topk; ++s) {
+            int32_t j = sparse_indices[(int64_t)i * topk + s];
+            if (j < 0 || j >= Tc) continue;
+            if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
+            rows[n] = j;
+            p[n] = attn_l1[(int64_t)i * topk + s];
+            mass += p[n];
+            double sc = 0.0;
+            for (int32_t h = 0; h < Hi; ++h) {
+                const double *qh = q + ((int64_t)i * Hi + h) * Di;
+                const double *kj = k + (int64_t)j * Di;
+                double dot = 0.0;
+                for (int32_t d = 0; d < Di; ++d) dot += qh[d] * kj[d];
+                dots[(int64_t)n * Hi + h] = dot;
+                sc += w[(int64_t)i * Hi + h] * (dot > 0.0 ? dot : 0.0);
+            }
+            score[n] = sc;
+            ++n;
+        }
+        if (n > 0 && mass > 0.0) {
+            /* log-softmax of the scores over S */
+            double mx = -INFINITY;
+            for (int32_t s = 0; s < n; ++s)
+                if (score[s] > mx) mx = score[s];
+            double z = 0.0;
+            for (int32_t s = 0; s < n; ++s) z += exp(score[s] - mx);
+            double lz = mx + log(z);
+            double kl = 0.0;
+            for (int32_t s = 0; s < n; ++s) {
+                double ps = p[s] / mass;
+                double log_pi = score[s] - lz;
+                if (ps > 0.0) kl += ps * (log(ps) - log_pi);
+                /* reuse score[] for g_s = dL/dI_s */
+                score[s] = grad_scale * (exp(log_pi) - ps);
+            }
+            loss[i] = kl;
+            for (int32_t s = 0; s < n; ++s) {
+                const double g = score[s];
+                const double *kj = k + (int64_t)rows[s] * Di;
+                double *gks = gk + (int64_t)s * Di;
+                for (int32_t d = 0; d < Di; ++d) gks[d] = 0.0;
+                for (int32_t h = 0; h < Hi; ++h) {
+                    double dot = dots[(int64_t)s * Hi + h];
+                    dw[h] += g * (dot > 0.0 ? dot : 0.0);
+                    if (!(dot > 0.0)) continue;
+                    double c = g * w[(int64_t)i * Hi + h];
+                    const double *qh = q + ((int64_t)i * Hi + h) * Di;
+                    double *dqh = dq + (int64_t)h * Di;
+                    for (int32_t d = 0; d < Di; ++d) {
+                        dqh[d] += c * kj[d];
+                        gks[d] += c * qh[d];
+                    }
+                }
+            }
+            if (d_k) {
+#pragma omp critical(csa_ref_kl_scatter)
+                for (int32_t s = 0; s < n; ++s)
+                    for (int32_t d = 0; d < Di; ++d)
+                        d_k[(int64_t)rows[s] * Di + d] += gk[(int64_t)s * Di + d];
+            }
+        }
+        free(rows), free(score), free(p), free(dots), free(gk);
     }
     return err;
 }
