@@ -197,3 +197,23 @@ def draw_pack(spec: PackSpec) -> list:
     """All layers of a pack, in order, from one generator seeded with ``spec.seed``."""
     gen = torch.Generator("cpu").manual_seed(spec.seed)
     return [draw_layer_tensors(spec, gen, layer) for layer in spec.layers]
+
+
+def draw_indexer_tensors(total_tokens: int, rows_c: int, index_heads: int, index_dim: int,
+                         seed: int, w_uniform: bool = False) -> dict:
+    """Indexer inputs alone (CPU): q_idx [T, Hi, Di] and k_idx [rows_c, Di] bf16
+    N(0,1), w [T, Hi] fp32 (N(0,1), or U(0,1) with ``w_uniform``), drawn in that
+    order from one generator seeded with ``seed``."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    bf16 = torch.bfloat16
+    out = {"q_idx": _randn(gen, (total_tokens, index_heads, index_dim), bf16),
+           "k_idx": _randn(gen, (rows_c, index_dim), bf16)}
+    out["w"] = (_rand(gen, (total_tokens, index_heads)) if w_uniform
+                else _randn(gen, (total_tokens, index_heads), torch.float32))
+    return out
+
+
+def draw_uniform(shape, seed: int, low: float = 0.0, high: float = 1.0) -> torch.Tensor:
+    """fp32 U(low, high) tensor (CPU) from a generator seeded with ``seed``."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return low + (high - low) * _rand(gen, tuple(shape))

@@ -12,10 +12,12 @@
  *   [hp#RFC]      "【RFC】DeepSeek-V4 CSA/HCA 自定义算子接入与对外接口对标
  *                 torch_extension" (hyper-parallel); sections 背景 (background),
  *                 1 npu_lightning_indexer, 2 npu_sparse_flash_mla,
+ *                 3 npu_sparse_lightning_indexer_kl_loss_grad,
  *                 4 npu_sparse_flash_mla_grad, 缺失入参的用途分析
  *                 (analysis of the missing arguments).
  *   [MS#4842]     MindSpeed-LLM PR 4842; section 主要改动 (main changes):
- *                 LayerCompressMode {NO_COMPRESS, COMPRESSOR_ONLY, INDEXER}.
+ *                 LayerCompressMode {NO_COMPRESS, COMPRESSOR_ONLY, INDEXER};
+ *                 the indexer loss's num_seqs (global token count) under TND.
  *   [MLM#7]       "feat(deepseek_v4): faithful THD context-parallel path for DS4
  *                 CSA" (verl Megatron-LM PR 7); section Environment note:
  *                 head_dim = d_v = 512.
@@ -228,6 +230,54 @@ csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, con
                                 int32_t ori_win_right, float *d_q, float *d_ori_kv,
                                 float *d_cmp_kv, float *d_sinks, float *ori_softmax_l1_norm,
                                 float *cmp_softmax_l1_norm, csa_stream_t stream);
+
+/*
+ * Indexer KL-loss gradient: the backward of the lightning indexer against the
+ * main attention's distribution.
+ * [hp#RFC] section 3 (sparse_lightning_indexer_kl_loss_grad(q, k, w,
+ * sparse_indices, attn_softmax_l1_norm, cu_seqlens_q, cu_seqlens_k,
+ * mask_mode=3, cmp_ratio): indexer backward plus KL loss, fed with the target
+ * distribution p that the attention backward returns as softmax_l1_norm);
+ * [MS#4842] (under TND the loss is normalised by the global token count:
+ * pass that factor as grad_scale). The pages give the arguments, not the
+ * loss; the reading taken: for token t, the entries s of sparse_indices[t]
+ * naming a row j_s in [0, Tc) visible to t (the indexer's causal rule) form
+ * its set S, and
+ *     I_s     = sum_h w[t,h] max(0, a_hs),  a_hs = q[t,h,:] . k[j_s,:]
+ *     p_s     = l1[t,s] / sum_{u in S} l1[t,u]
+ *     loss[t] = sum_{s in S, p_s > 0} p_s (log p_s - log softmax_S(I)_s)
+ * (KL(p || softmax of the indexer scores) over the selected rows). Outputs
+ * are the gradients of L = grad_scale * sum_t loss[t] (p is a target):
+ *     g_s         = grad_scale (softmax_S(I)_s - p_s)
+ *     d_w[t,h]    = sum_s g_s max(0, a_hs)
+ *     d_q[t,h,:]  = sum_s g_s w[t,h] [a_hs > 0] k[j_s,:]
+ *     d_k[j_s,:] += g_s sum_h w[t,h] [a_hs > 0] q[t,h,:]
+ * A token with no entry in S, or whose entries carry no mass, gets loss 0
+ * and zero gradients. Each entry counts on its own.
+ * q [T, Hi, Di] bf16; k [Tc, Di] bf16; w [T, Hi] fp32;
+ * sparse_indices [T, topk] int32 (e.g. csa_indexer_topk's output);
+ * attn_softmax_l1_norm [T, topk] fp32 (e.g. csa_sparse_mla_bwd's
+ * cmp_softmax_l1_norm for the same list); cu_seqlens_q, cu_seqlens_cmp_kv
+ * [batch+1] int32 as for csa_indexer_topk.
+ * Outputs, fp32, overwritten: d_q [T, Hi, Di], d_k [Tc, Di], d_w [T, Hi],
+ * loss [T] (unscaled KL per token; may be NULL). d_k is a sum over tokens
+ * made with fp32 atomics, so its last bits depend on the order the tokens
+ * finish in.
+ * Errors: negative sizes or topk < 1 -> CSA_ERR_SHAPE; Di not in {64, 128},
+ * Hi not in [1, 64], cmp_ratio < 2, topk > 2048 -> CSA_ERR_UNSUPPORTED;
+ * NULL inputs or outputs (k and d_k may be NULL only when Tc == 0) ->
+ * CSA_ERR_NULL; q, k and d_k must be 16-byte aligned (else
+ * CSA_ERR_UNSUPPORTED). total_tokens == 0 launches nothing.
+ */
+csa_status_t csa_indexer_kl_loss_grad(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                                      const int32_t *sparse_indices,
+                                      const float *attn_softmax_l1_norm, int32_t total_tokens,
+                                      int32_t total_cmp, int32_t index_heads, int32_t index_dim,
+                                      const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                      int32_t cmp_ratio, int32_t topk, float grad_scale,
+                                      float *d_q, float *d_k, float *d_w, float *loss,
+                                      csa_stream_t stream);
 
 /*
  * csa_indexer_topk without a workspace, for callers that cannot allocate

@@ -43,7 +43,7 @@ def lib():
             C.c_double, i32, i32, f64p, f64p, f64p, f64p, f64p, f64p]
         _lib.csa_ref_indexer_kl_loss_grad.argtypes = [
             f64p, f64p, f64p, i32p, f64p, i32, i32, i32, i32, i32, i32p, i32p, i32, i32,
-            C.c_double, i32p, i32, f64p, f64p, f64p, f64p]
+            C.c_double, i32p, i32, f64p, f64p, f64p, f64p, f64p]
         for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx",
                      "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd",
                      "csa_ref_indexer_kl_loss_grad"):
@@ -195,8 +195,9 @@ def indexer_kl_loss_grad(q_rows, k, w_rows, sparse_indices, attn_l1, total_token
     """KL loss of the indexer against the attention distribution, and its
     gradients, in fp64. ``q_rows``, ``w_rows``, ``sparse_indices`` and
     ``attn_l1`` hold one row per listed token (all tokens when ``tokens`` is
-    None). Returns a dict: loss [n], d_q [n,Hi,Di], d_w [n,Hi] and d_k [Tc,Di]
-    (the listed tokens' contributions; None unless ``want_dk``)."""
+    None). Returns a dict: loss [n], d_q [n,Hi,Di], d_w [n,Hi], d_k [Tc,Di]
+    (the listed tokens' contributions; None unless ``want_dk``) and g [n,topk]
+    (dL/dI per list entry, zero where the entry is skipped)."""
     q = _f64(q_rows)
     w = _f64(w_rows)
     kk = _f64(k)
@@ -210,11 +211,11 @@ def indexer_kl_loss_grad(q_rows, k, w_rows, sparse_indices, attn_l1, total_token
     if kk is not None and kk.size == 0:
         kk = None
     res = {"loss": np.zeros(n), "d_q": np.zeros((n, hi, di)), "d_w": np.zeros((n, hi)),
-           "d_k": np.zeros((tc, di)) if want_dk else None}
+           "d_k": np.zeros((tc, di)) if want_dk else None, "g": np.zeros((n, topk))}
     _check(lib().csa_ref_indexer_kl_loss_grad(
         _p(q, C.c_double), _p(kk, C.c_double), _p(w, C.c_double), _p(idx, C.c_int32),
         _p(a, C.c_double), total_tokens, tc, hi, di, topk, _p(cu, C.c_int32),
         _p(cuc, C.c_int32), len(cu) - 1, cmp_ratio, float(grad_scale), _p(tok, C.c_int32), n,
         _p(res["d_q"], C.c_double), _p(res["d_k"], C.c_double), _p(res["d_w"], C.c_double),
-        _p(res["loss"], C.c_double)), "indexer_kl_loss_grad")
+        _p(res["loss"], C.c_double), _p(res["g"], C.c_double)), "indexer_kl_loss_grad")
     return res

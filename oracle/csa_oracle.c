@@ -529,6 +529,8 @@ int csa_ref_sparse_mla_bwd(const double *q, const double *dout, const double *or
  * Rows of q, w, sparse_indices, attn_l1, d_q, d_w and loss are per listed
  * token (tokens == NULL: all T tokens, row i is token i); d_k [Tc, Di] is
  * overwritten with the contributions of the listed tokens (may be NULL).
+ * g_out (may be NULL) receives dL/dI_s per list entry, [n_tokens, topk],
+ * zero for skipped entries.
  */
 int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double *w,
                                  const int32_t *sparse_indices, const double *attn_l1, int32_t T,
@@ -536,7 +538,7 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
                                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp,
                                  int32_t batch, int32_t cmp_ratio, double grad_scale,
                                  const int32_t *tokens, int32_t n_tokens, double *d_q, double *d_k,
-                                 double *d_w, double *loss) {
+                                 double *d_w, double *loss, double *g_out) {
     if (!q || !w || !sparse_indices || !attn_l1 || !cu_seqlens || !cu_seqlens_cmp) return REF_ERR_ARG;
     if (!d_q || !d_w || !loss) return REF_ERR_ARG;
     if (Tc > 0 && !k) return REF_ERR_ARG;
@@ -554,18 +556,21 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
         for (int64_t e = 0; e < (int64_t)Hi * Di; ++e) dq[e] = 0.0;
         for (int32_t h = 0; h < Hi; ++h) dw[h] = 0.0;
         loss[i] = 0.0;
+        if (g_out)
+            for (int32_t s = 0; s < topk; ++s) g_out[(int64_t)i * topk + s] = 0.0;
         if (t < 0 || t >= T) {
             err = REF_ERR_ARG;
             continue;
         }
         int32_t b = segment_of(cu_seqlens, batch, t);
         int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk);
+        int32_t *slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk);
         double *score = (double *)malloc(sizeof(double) * (size_t)topk);
         double *p = (double *)malloc(sizeof(double) * (size_t)topk);
         double *dots = (double *)malloc(sizeof(double) * (size_t)topk * (size_t)Hi);
         double *gk = (double *)malloc(sizeof(double) * (size_t)topk * (size_t)Di);
-        if (!rows || !score || !p || !dots || !gk) {
-            free(rows), free(score), free(p), free(dots), free(gk);
+        if (!rows || !slot || !score || !p || !dots || !gk) {
+            free(rows), free(slot), free(score), free(p), free(dots), free(gk);
             err = REF_ERR_NOMEM;
             continue;
         }
@@ -577,6 +582,7 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
             if (j < 0 || j >= Tc) continue;
             if (!block_visible(cu_seqlens, cu_seqlens_cmp, b, t, cmp_ratio, j)) continue;
             rows[n] = j;
+            slot[n] = s;
             p[n] = attn_l1[(int64_t)i * topk + s];
             mass += p[n];
             double sc = 0.0;
@@ -606,6 +612,7 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
                 if (ps > 0.0) kl += ps * (log(ps) - log_pi);
                 /* reuse score[] for g_s = dL/dI_s */
                 score[s] = grad_scale * (exp(log_pi) - ps);
+                if (g_out) g_out[(int64_t)i * topk + slot[s]] = score[s];
             }
             loss[i] = kl;
             for (int32_t s = 0; s < n; ++s) {
@@ -633,7 +640,7 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
                         d_k[(int64_t)rows[s] * Di + d] += gk[(int64_t)s * Di + d];
             }
         }
-        free(rows), free(score), free(p), free(dots), free(gk);
+        free(rows), free(slot), free(score), free(p), free(dots), free(gk);
     }
     return err;
 }

@@ -22,7 +22,7 @@ __all__ = [
     "CsaError", "lib", "library_path", "csa_status_string", "csa_compress_cu_seqlens",
     "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
     "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
-    "EXPORTED_SYMBOLS",
+    "csa_indexer_kl_loss_grad", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "csa_status_string", "csa_compress_cu_seqlens", "csa_window_idx",
     "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
     "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
+    "csa_indexer_kl_loss_grad",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -76,9 +77,12 @@ def lib():
         L.csa_device_error.argtypes = [_vp, C.POINTER(_i32)]
         L.csa_indexer_topk_noalloc.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp,
                                                _i32, _i32, _i32, _vp, _vp, _vp]
+        L.csa_indexer_kl_loss_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                               _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
+                                               _vp, _vp]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
                      "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error",
-                     "csa_indexer_topk_noalloc"):
+                     "csa_indexer_topk_noalloc", "csa_indexer_kl_loss_grad"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -280,6 +284,40 @@ def csa_sparse_mla_bwd(q, dout, out, lse, ori_kv, cmp_kv, cmp_sparse_indices, cu
         float(softmax_scale), int(cmp_ratio), int(ori_win_left), int(ori_win_right),
         _ptr(res["d_q"]), _ptr(res["d_ori_kv"]), _ptr(res["d_cmp_kv"]), _ptr(res["d_sinks"]),
         _ptr(res["ori_l1"]), _ptr(res["cmp_l1"]), _stream(stream)), "csa_sparse_mla_bwd")
+    return res
+
+
+def csa_indexer_kl_loss_grad(q, k, w, sparse_indices, attn_softmax_l1_norm, cu_seqlens_q,
+                             cu_seqlens_cmp_kv, cmp_ratio: int, grad_scale: float = 1.0,
+                             want_loss: bool = True, stream=None):
+    """Indexer KL loss against the attention distribution, and its gradients.
+
+    Returns a dict of fp32 tensors: d_q [T,Hi,Di], d_k [Tc,Di] (None when
+    Tc == 0), d_w [T,Hi] and loss [T] (the unscaled KL per token; None unless
+    ``want_loss``). The gradients are those of ``grad_scale * loss.sum()``."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(sparse_indices, "sparse_indices", torch.int32, 2)
+    _need(attn_softmax_l1_norm, "attn_softmax_l1_norm", torch.float32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_cmp_kv, "cu_seqlens_cmp_kv", torch.int32, 1)
+    T, Hi, Di = q.shape
+    Tc = 0 if k is None else k.shape[0]
+    topk = sparse_indices.shape[1]
+    if tuple(attn_softmax_l1_norm.shape) != (T, topk) or sparse_indices.shape[0] != T:
+        raise ValueError("sparse_indices and attn_softmax_l1_norm must both be [T, topk]")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    res = {"d_q": torch.empty((T, Hi, Di), **f32),
+           "d_k": torch.empty((Tc, Di), **f32) if Tc else None,
+           "d_w": torch.empty((T, Hi), **f32),
+           "loss": torch.empty((T,), **f32) if want_loss else None}
+    _check(lib().csa_indexer_kl_loss_grad(
+        _ptr(q), _ptr(k) if Tc else None, _ptr(w), _ptr(sparse_indices),
+        _ptr(attn_softmax_l1_norm), T, Tc, Hi, Di, _ptr(cu_seqlens_q), _ptr(cu_seqlens_cmp_kv),
+        cu_seqlens_q.numel() - 1, int(cmp_ratio), int(topk), float(grad_scale), _ptr(res["d_q"]),
+        _ptr(res["d_k"]), _ptr(res["d_w"]), _ptr(res["loss"]), _stream(stream)),
+        "csa_indexer_kl_loss_grad")
     return res
 
 

@@ -22,6 +22,7 @@ enum KernelId : int32_t {
     kKerIndexer = 3,
     kKerMla = 4,
     kKerMlaBwd = 5,
+    kKerIndexerKl = 6,
 };
 
 __device__ __forceinline__ void report_error(int32_t *err, int32_t kind, int32_t kernel,

@@ -253,6 +253,55 @@ csa_status_t csa_sparse_mla_fwd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
     return from_cuda(csa::launch_sparse_mla_fwd(a, (cudaStream_t)stream));
 }
 
+csa_status_t csa_indexer_kl_loss_grad(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                                      const int32_t *sparse_indices,
+                                      const float *attn_softmax_l1_norm, int32_t total_tokens,
+                                      int32_t total_cmp, int32_t index_heads, int32_t index_dim,
+                                      const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_cmp_kv, int32_t batch,
+                                      int32_t cmp_ratio, int32_t topk, float grad_scale,
+                                      float *d_q, float *d_k, float *d_w, float *loss,
+                                      csa_stream_t stream) {
+    if (total_tokens < 0 || total_cmp < 0 || batch < 0 || topk < 1) return CSA_ERR_SHAPE;
+    if (index_dim != 64 && index_dim != 128) return CSA_ERR_UNSUPPORTED;
+    if (index_heads < 1 || index_heads > 64) return CSA_ERR_UNSUPPORTED;
+    if (cmp_ratio < 2) return CSA_ERR_UNSUPPORTED;
+    if (topk > csa::indexer_kl_max_topk()) return CSA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return CSA_OK;  // nothing to do (empty buffers may be NULL)
+    if (!q || !w || !sparse_indices || !attn_softmax_l1_norm || !cu_seqlens_q ||
+        !cu_seqlens_cmp_kv || !d_q || !d_w)
+        return CSA_ERR_NULL;
+    if (total_cmp > 0 && (!k || !d_k)) return CSA_ERR_NULL;
+    // 16-byte loads of q / k rows and 16-byte atomic adds into d_k
+    if (((uintptr_t)q & 15u) || (k && ((uintptr_t)k & 15u)) || (d_k && ((uintptr_t)d_k & 15u)))
+        return CSA_ERR_UNSUPPORTED;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    csa::IndexerKlArgs a;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.k = total_cmp > 0 ? reinterpret_cast<const __nv_bfloat16 *>(k) : nullptr;
+    a.w = w;
+    a.idx = sparse_indices;
+    a.l1 = attn_softmax_l1_norm;
+    a.cu_q = cu_seqlens_q;
+    a.cu_c = cu_seqlens_cmp_kv;
+    a.d_q = d_q;
+    a.d_k = total_cmp > 0 ? d_k : nullptr;
+    a.d_w = d_w;
+    a.loss = loss;
+    a.err = err;
+    a.T = total_tokens;
+    a.Tc = total_cmp;
+    a.Hi = index_heads;
+    a.Di = index_dim;
+    a.batch = batch;
+    a.cmp_ratio = cmp_ratio;
+    a.topk = topk;
+    a.grad_scale = grad_scale;
+    return from_cuda(csa::launch_indexer_kl_grad(a, (cudaStream_t)stream));
+}
+
 csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail) {
     csa_status_t st;
     int32_t *err = error_word(&st);

@@ -83,6 +83,27 @@ cudaError_t launch_sparse_mla_bwd_tc(const MlaBwdArgs &a, cudaStream_t stream);
 // Largest topk (entries of cmp_sparse_indices per token) the kernel accepts.
 int32_t sparse_mla_max_topk();
 
+struct IndexerKlArgs {
+    const __nv_bfloat16 *q;  // [T, Hi, Di]
+    const __nv_bfloat16 *k;  // [Tc, Di] (nullptr when Tc == 0)
+    const float *w;          // [T, Hi]
+    const int32_t *idx;      // [T, topk] sparse_indices
+    const float *l1;         // [T, topk] attn_softmax_l1_norm
+    const int32_t *cu_q;     // [batch+1]
+    const int32_t *cu_c;     // [batch+1]
+    float *d_q;              // [T, Hi, Di]
+    float *d_k;              // [Tc, Di]
+    float *d_w;              // [T, Hi]
+    float *loss;             // [T] or nullptr
+    int32_t *err;
+    int32_t T, Tc, Hi, Di, batch, cmp_ratio, topk;
+    float grad_scale;
+};
+
+cudaError_t launch_indexer_kl_grad(const IndexerKlArgs &a, cudaStream_t stream);
+// Largest topk (entries of sparse_indices per token) the kernel accepts.
+int32_t indexer_kl_max_topk();
+
 // Device error word of the current device (csa_api.cu).
 int32_t *device_error_word(csa_status_t *st);
 

@@ -146,6 +146,32 @@ def test_mla_bwd_rejects(L):
     assert call(dokv=C.c_void_p(0x1004)) == 3
 
 
+def test_indexer_kl_rejects(L):
+    names = ["q", "k", "w", "idx", "l1", "T", "Tc", "Hi", "Di", "cuq", "cuc", "batch", "r",
+             "topk", "gs", "dq", "dk", "dw", "loss", "stream"]
+    base = dict(q=P, k=P, w=P, idx=P, l1=P, T=256, Tc=63, Hi=4, Di=64, cuq=P, cuc=P, batch=3,
+                r=4, topk=8, gs=C.c_float(1.0 / 256), dq=P, dk=P, dw=P, loss=P, stream=NUL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.csa_indexer_kl_loss_grad(*[a[n] for n in names])
+
+    for k in ("q", "k", "w", "idx", "l1", "cuq", "cuc", "dq", "dk", "dw"):
+        assert call(**{k: NUL}) == 1, k
+    assert call(T=-1) == 2
+    assert call(Tc=-1) == 2
+    assert call(topk=0) == 2
+    assert call(Di=96) == 3
+    assert call(Hi=0) == 3
+    assert call(Hi=65) == 3
+    assert call(r=1) == 3
+    assert call(topk=2049) == 3
+    assert call(q=C.c_void_p(0x1002)) == 3  # 16-byte alignment
+    assert call(dk=C.c_void_p(0x1004)) == 3
+    assert call(T=0) == 0  # nothing to do, nothing launched
+
+
 def test_product_does_not_import_oracle():
     pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
     for dirpath, _, files in os.walk(pkg):

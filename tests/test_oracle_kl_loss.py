@@ -190,3 +190,24 @@ def test_invariances():
     res2 = run(c, scale=2 * GRAD_SCALE)
     np.testing.assert_allclose(res2["d_q"], 2 * base["d_q"], rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(res2["loss"], base["loss"], rtol=1e-12, atol=1e-15)
+
+
+def test_score_gradient_output():
+    """g = dL/dI per entry: it sums to zero over a token's entries (softmax
+    minus a normalised target), vanishes on skipped entries, and gives back
+    the finite-difference-pinned d_w through sum_s g_s relu(q . k)."""
+    c = make_case(8)
+    res = run(c)
+    g = res["g"]
+    dots = np.einsum("thd,jd->thj", c["q"], c["k"])
+    for t in range(c["T"]):
+        S = entry_set(c, t)
+        skipped = [s for s in range(TOPK) if s not in S]
+        assert (g[t, skipped] == 0).all()
+        if not S:
+            continue
+        assert abs(g[t].sum()) < 1e-12
+        rows = c["idx"][t, S]
+        want = (g[t, S][None, :] * np.maximum(dots[t][:, rows], 0)).sum(1)
+        np.testing.assert_allclose(res["d_w"][t], want, rtol=1e-12, atol=1e-14)
+    assert np.abs(g).max() > 0.01
