@@ -24,9 +24,11 @@ Extra objects on the JSON line:
 * clocks    -- nvidia-smi samples taken during the timed region.
 
 ``--impl reference`` times the oracle itself as the step (a bounded token
-sample per step) on the host cores. ``--bwd`` adds a second JSON line: the
-sparse MLA backward of every layer, timed per launch from the forward's out
-and lse, with its FLOPs against the bf16 tensor peak.
+sample per step) on the host cores. ``--bwd`` adds a JSON line: the sparse
+MLA backward of every layer, timed per launch from the forward's out and
+lse, with its FLOPs against the bf16 tensor peak. ``--kl`` adds one more: the
+indexer KL-loss gradient of the indexer layer, on its own top-k rows with
+the attention backward's distribution as target, against the fp32 ALU peak.
 """
 
 from __future__ import annotations
@@ -72,6 +74,9 @@ def parse_args():
                    help="also time the sparse MLA backward of every layer and print its own "
                         "JSON line after the forward's (off by default: one line per run)")
     p.add_argument("--bwd-steps", type=int, default=5)
+    p.add_argument("--kl", action="store_true",
+                   help="also time the indexer KL-loss gradient of each indexer layer "
+                        "(one more JSON line)")
     return p.parse_args()
 
 
@@ -125,6 +130,7 @@ def layer_accounting(spec, layer):
     W = spec.win_left + 1
     keys = 0
     nvis_sum = 0
+    cmp_keys = 0
     for L in spec.lengths:
         pos = np.arange(L, dtype=np.int64)
         win = np.minimum(W, pos + 1)
@@ -132,9 +138,11 @@ def layer_accounting(spec, layer):
         cmp = np.minimum(layer.topk, nvis) if layer.indexer else nvis
         keys += int(win.sum() + cmp.sum())
         nvis_sum += int(nvis.sum())
+        cmp_keys += int(cmp.sum())
     D, H = spec.dim, spec.heads
     acc = {
         "keys": keys,
+        "cmp_keys": cmp_keys,
         "kv_bytes": keys * D * 2,
         "mla_flops": 4 * D * H * keys,
         "idx_flops": (2 * layer.index_heads * layer.index_dim * nvis_sum) if layer.indexer else 0,
@@ -466,7 +474,82 @@ def run_ours(args, world, rank, local):
         result["cpu_baseline"] = cpu_baseline(layers, args.cpu_seconds)
     if args.bwd and rank == 0:
         result["_bwd"] = run_bwd(args, layers, stream, flush, peaks, peak_kind)
+    if args.kl and rank == 0:
+        result["_kl"] = run_kl(args, layers, stream, flush)
     return result
+
+
+def fp32_alu_peak_tflops():
+    """FP32 FMA peak of the CUDA cores from unit counts and the maximum SM
+    clock: SMs x 128 fp32 lanes x 2 FLOP per FMA x clock."""
+    peaks, _ = load_peaks()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"{sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
+
+
+def run_kl(args, layers, stream, flush):
+    """The indexer KL-loss gradient of each indexer layer, on that layer's own
+    top-k rows with the attention backward's head-averaged distribution over
+    them (cmp_softmax_l1_norm) as the target, timed per launch with CUDA
+    events between L2 flushes. Algorithmic FLOPs per (token, listed row):
+    2 Hi Di each for the score, d_q and d_k -> 6 Hi Di (fp32 CUDA cores)."""
+    import sparse_attention_csa_gb300 as csa
+    gen = torch.Generator().manual_seed(8)
+    per, flops, entries = {}, 0, 0
+    for L in layers:
+        if not L.layer.indexer:
+            continue
+        spec, r = L.spec, L.layer.cmp_ratio
+        T = spec.total_tokens
+        dout = torch.randn(tuple(L.out.shape), generator=gen).to(torch.bfloat16).to(L.out.device)
+        L.launches(stream)
+        bwd = csa.csa_sparse_mla_bwd(L.dev["q"], dout, L.out, L.lse, L.dev["ori_kv"],
+                                     L.dev["cmp_kv"], L.idx, L.dev["cu"], L.dev["cu"], L.cuc,
+                                     L.dev["sinks"], spec.scale, r, spec.win_left, stream=stream)
+        l1 = bwd["cmp_l1"]
+        del bwd, dout
+
+        def call():
+            return csa.csa_indexer_kl_loss_grad(L.dev["q_idx"], L.dev["k_idx"], L.dev["w"], L.idx,
+                                                l1, L.dev["cu"], L.cuc, r, 1.0 / T,
+                                                stream=stream)
+
+        for _ in range(2):
+            flush.zero_()
+            call()
+        ms = []
+        for _ in range(args.bwd_steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        per[f"indexer_kl_grad/r{r}"] = statistics.median(ms)
+        hi, di = L.layer.index_heads, L.layer.index_dim
+        flops += 6 * hi * di * L.acc["cmp_keys"]
+        entries += L.acc["cmp_keys"]
+    st, word = csa.csa_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the KL gradient: {word:#x}")
+    total = sum(per.values())
+    spec = layers[0].spec
+    achieved = flops / (total * 1e-3) / 1e12
+    peak, how = fp32_alu_peak_tflops()
+    return {
+        "metric": "indexer KL-loss gradient tokens/s (loss, d_q, d_k, d_w) on 1 GB300",
+        "value": spec.total_tokens / (total * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.bwd_steps, "warmup": 2, "ms_per_step": total, "higher_is_better": True,
+        "dtype": "f32 (CUDA cores, from bf16 inputs)", "data": "synthetic", "part": "indexer KL",
+        "config": {"workload": f"{spec.name}, indexer layers, own top-k rows, attention "
+                               "distribution as target", "list_entries": entries,
+                   "l2": "flushed between launches"},
+        "kernels_ms": per,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": how, "flops": flops},
+    }
 
 
 def run_bwd(args, layers, stream, flush, peaks, peak_src):
@@ -628,10 +711,12 @@ def main():
     world, rank, local = dist_setup("nccl")
     res = run_ours(args, world, rank, local)
     bwd = res.pop("_bwd", None)
+    kl = res.pop("_kl", None)
     if rank == 0:
         print(json.dumps(res), flush=True)
-        if bwd is not None:
-            print(json.dumps(bwd), flush=True)
+        for extra in (bwd, kl):
+            if extra is not None:
+                print(json.dumps(extra), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

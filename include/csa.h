@@ -280,6 +280,66 @@ csa_status_t csa_indexer_kl_loss_grad(const csa_bf16_t *q, const csa_bf16_t *k, 
                                       csa_stream_t stream);
 
 /*
+ * BSND layout (fixed-shape batch) of the forward path.
+ * [hp#RFC] sections 1 and 2: the ops take a layout argument whose default is
+ * "BSND" -- q [B, S, N, D], KV [B, S_kv, 1, D], compressed indices local to
+ * their batch -- and seqused_q / seqused_kv declaring how many leading rows
+ * of each batch are valid (rows past them are left unspecified). Here one
+ * seqused array serves q and both KV streams (self-attention prefill: the
+ * query rows are the KV rows), and the compressed stream of batch b holds
+ * min(floor(seqused[b] / cmp_ratio), seqlen_cmp) valid rows.
+ * The computation is exactly the THD one applied to each batch's valid rows
+ * as one sequence: a valid row p of batch b sees the window rows
+ * [max(0, p - ori_win_left), p] of its batch and the compressed rows j
+ * (batch-local) with (j + 1) * cmp_ratio <= p + 1.
+ * Implementation: batch b is rows [b S, (b+1) S) of the packed THD stream;
+ * the call writes, in the caller's workspace, THD offsets with two sequences
+ * per batch (valid rows, then padding rows) and the stream-absolute form of
+ * the compressed indices, then runs the THD kernels. Outputs of padding rows
+ * (p >= seqused[b]) are unspecified.
+ * seqused [B] int32 (device) or NULL (every row valid); entries outside
+ * [0, seqlen] are clamped and recorded in the device error word.
+ *
+ * csa_bsnd_mla_workspace_size: bytes of workspace csa_sparse_mla_fwd_bsnd
+ * needs (topk = 0 when no index list is passed).
+ * csa_sparse_mla_fwd_bsnd: as csa_sparse_mla_fwd, with q [B, S, H, D],
+ *   ori_kv [B, S, D], cmp_kv [B, Sc, D] or NULL, cmp_sparse_indices
+ *   [B, S, topk] batch-local rows (-1 or outside [0, Sc): skipped) or NULL
+ *   (every visible compressed row), out [B, S, H, D], softmax_lse [B, S, H].
+ *   workspace: at least csa_bsnd_mla_workspace_size(B, S, topk) bytes,
+ *   256-byte aligned. Errors as csa_sparse_mla_fwd, plus B * S or B * Sc
+ *   above INT32_MAX -> CSA_ERR_SHAPE and a short or misaligned workspace ->
+ *   CSA_ERR_WORKSPACE. B * S == 0 launches nothing.
+ * csa_bsnd_indexer_workspace_size / csa_indexer_topk_bsnd: as
+ *   csa_indexer_topk with q [B, S, Hi, Di], k [B, Sc, Di], w [B, S, Hi];
+ *   topk_idx [B, S, topk] receives batch-local rows (-1 padded), topk_val
+ *   [B, S, topk] or NULL. The workspace also holds the indexer's own score
+ *   spill. Errors as csa_indexer_topk, plus the shape and workspace checks
+ *   above.
+ */
+size_t csa_bsnd_mla_workspace_size(int32_t batch, int32_t seqlen, int32_t topk);
+
+csa_status_t csa_sparse_mla_fwd_bsnd(const csa_bf16_t *q, const csa_bf16_t *ori_kv,
+                                     const csa_bf16_t *cmp_kv, const int32_t *cmp_sparse_indices,
+                                     const int32_t *seqused, int32_t batch, int32_t seqlen,
+                                     int32_t seqlen_cmp, int32_t heads, int32_t head_dim,
+                                     int32_t topk, const float *sinks, float softmax_scale,
+                                     int32_t cmp_ratio, int32_t ori_win_left,
+                                     int32_t ori_win_right, csa_bf16_t *out, float *softmax_lse,
+                                     int32_t return_softmax_lse, void *workspace,
+                                     size_t workspace_bytes, csa_stream_t stream);
+
+size_t csa_bsnd_indexer_workspace_size(int32_t batch, int32_t seqlen, int32_t seqlen_cmp,
+                                       int32_t index_heads, int32_t index_dim, int32_t topk);
+
+csa_status_t csa_indexer_topk_bsnd(const csa_bf16_t *q, const csa_bf16_t *k, const float *w,
+                                   const int32_t *seqused, int32_t batch, int32_t seqlen,
+                                   int32_t seqlen_cmp, int32_t index_heads, int32_t index_dim,
+                                   int32_t cmp_ratio, int32_t topk, int32_t *topk_idx,
+                                   float *topk_val, void *workspace, size_t workspace_bytes,
+                                   csa_stream_t stream);
+
+/*
  * csa_indexer_topk without a workspace, for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point.
  *

@@ -22,7 +22,8 @@ __all__ = [
     "CsaError", "lib", "library_path", "csa_status_string", "csa_compress_cu_seqlens",
     "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
     "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
-    "csa_indexer_kl_loss_grad", "EXPORTED_SYMBOLS",
+    "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
+    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +34,8 @@ EXPORTED_SYMBOLS = (
     "csa_status_string", "csa_compress_cu_seqlens", "csa_window_idx",
     "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
     "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
-    "csa_indexer_kl_loss_grad",
+    "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
+    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -80,9 +82,19 @@ def lib():
         L.csa_indexer_kl_loss_grad.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                                _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
                                                _vp, _vp]
+        L.csa_bsnd_mla_workspace_size.restype = _sz
+        L.csa_bsnd_mla_workspace_size.argtypes = [_i32] * 3
+        L.csa_sparse_mla_fwd_bsnd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                              _i32, _i32, _vp, _f32, _i32, _i32, _i32, _vp, _vp,
+                                              _i32, _vp, _sz, _vp]
+        L.csa_bsnd_indexer_workspace_size.restype = _sz
+        L.csa_bsnd_indexer_workspace_size.argtypes = [_i32] * 6
+        L.csa_indexer_topk_bsnd.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                            _i32, _i32, _vp, _vp, _vp, _sz, _vp]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
                      "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error",
-                     "csa_indexer_topk_noalloc", "csa_indexer_kl_loss_grad"):
+                     "csa_indexer_topk_noalloc", "csa_indexer_kl_loss_grad",
+                     "csa_sparse_mla_fwd_bsnd", "csa_indexer_topk_bsnd"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -319,6 +331,75 @@ def csa_indexer_kl_loss_grad(q, k, w, sparse_indices, attn_softmax_l1_norm, cu_s
         _ptr(res["d_k"]), _ptr(res["d_w"]), _ptr(res["loss"]), _stream(stream)),
         "csa_indexer_kl_loss_grad")
     return res
+
+
+def _workspace(need, device, workspace):
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    size = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return workspace, size
+
+
+def csa_sparse_mla_fwd_bsnd(q, ori_kv, cmp_kv, cmp_sparse_indices, seqused, sinks,
+                            softmax_scale: float, cmp_ratio: int, ori_win_left: int,
+                            ori_win_right: int = 0, return_softmax_lse: bool = False,
+                            workspace=None, out=None, lse=None, stream=None):
+    """Sparse MLA forward in BSND layout: q [B,S,H,D], ori_kv [B,S,D], cmp_kv
+    [B,Sc,D] or None, cmp_sparse_indices [B,S,topk] batch-local or None,
+    seqused [B] int32 or None. Returns ``(out [B,S,H,D], lse [B,S,H] or None)``;
+    rows past seqused are unspecified."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(ori_kv, "ori_kv", torch.bfloat16, 3)
+    _need(cmp_kv, "cmp_kv", torch.bfloat16, 3)
+    _need(cmp_sparse_indices, "cmp_sparse_indices", torch.int32, 3)
+    _need(seqused, "seqused", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    B, S, H, D = q.shape
+    Sc = 0 if cmp_kv is None else cmp_kv.shape[1]
+    topk = 0 if cmp_sparse_indices is None else cmp_sparse_indices.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if return_softmax_lse and lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    list_used = topk if Sc else 0
+    need = int(lib().csa_bsnd_mla_workspace_size(B, S, list_used))
+    workspace, ws_bytes = _workspace(need, q.device, workspace)
+    _check(lib().csa_sparse_mla_fwd_bsnd(
+        _ptr(q), _ptr(ori_kv), _ptr(cmp_kv) if Sc else None, _ptr(cmp_sparse_indices),
+        _ptr(seqused), B, S, Sc, H, D, topk, _ptr(sinks), float(softmax_scale), int(cmp_ratio),
+        int(ori_win_left), int(ori_win_right), _ptr(out),
+        _ptr(lse) if return_softmax_lse else None, 1 if return_softmax_lse else 0,
+        _ptr(workspace), ws_bytes, _stream(stream)), "csa_sparse_mla_fwd_bsnd")
+    return out, (lse if return_softmax_lse else None)
+
+
+def csa_indexer_topk_bsnd(q, k, w, seqused, cmp_ratio: int, topk: int,
+                          return_value: bool = False, workspace=None, out=None, out_val=None,
+                          stream=None):
+    """Lightning-indexer top-k in BSND layout: q [B,S,Hi,Di], k [B,Sc,Di],
+    w [B,S,Hi], seqused [B] int32 or None. Returns ``(topk_idx [B,S,topk]
+    batch-local rows, topk_val or None)``; rows past seqused are unspecified."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(w, "w", torch.float32, 3)
+    _need(seqused, "seqused", torch.int32, 1)
+    B, S, Hi, Di = q.shape
+    Sc = 0 if k is None else k.shape[1]
+    if out is None:
+        out = torch.empty((B, S, topk), dtype=torch.int32, device=q.device)
+    if return_value and out_val is None:
+        out_val = torch.empty((B, S, topk), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.int32, 3)
+    _need(out_val, "out_val", torch.float32, 3)
+    need = int(lib().csa_bsnd_indexer_workspace_size(B, S, Sc, Hi, Di, int(topk)))
+    workspace, ws_bytes = _workspace(need, q.device, workspace)
+    _check(lib().csa_indexer_topk_bsnd(
+        _ptr(q), _ptr(k) if Sc else None, _ptr(w), _ptr(seqused), B, S, Sc, Hi, Di,
+        int(cmp_ratio), int(topk), _ptr(out), _ptr(out_val) if return_value else None,
+        _ptr(workspace), ws_bytes, _stream(stream)), "csa_indexer_topk_bsnd")
+    return out, (out_val if return_value else None)
 
 
 def csa_device_error(stream=None):

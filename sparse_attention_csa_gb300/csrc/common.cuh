@@ -23,6 +23,7 @@ enum KernelId : int32_t {
     kKerMla = 4,
     kKerMlaBwd = 5,
     kKerIndexerKl = 6,
+    kKerBsnd = 7,
 };
 
 __device__ __forceinline__ void report_error(int32_t *err, int32_t kind, int32_t kernel,

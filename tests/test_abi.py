@@ -172,6 +172,59 @@ def test_indexer_kl_rejects(L):
     assert call(T=0) == 0  # nothing to do, nothing launched
 
 
+def test_bsnd_rejects(L):
+    names = ["q", "okv", "ckv", "idx", "su", "B", "S", "Sc", "H", "D", "topk", "sinks", "scale",
+             "r", "wl", "wr", "out", "lse", "ret", "ws", "wsb", "stream"]
+    need = L.csa_bsnd_mla_workspace_size(3, 200, 16)
+    assert need >= 3 * 200 * 16 * 4
+    assert L.csa_bsnd_mla_workspace_size(3, 200, 0) < need
+    base = dict(q=P, okv=P, ckv=P, idx=P, su=NUL, B=3, S=200, Sc=50, H=8, D=512, topk=16,
+                sinks=P, scale=C.c_float(0.044), r=4, wl=31, wr=0, out=P, lse=P, ret=1,
+                ws=C.c_void_p(0x10000), wsb=need, stream=NUL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.csa_sparse_mla_fwd_bsnd(*[a[n] for n in names])
+
+    for k in ("q", "okv", "out", "lse"):
+        assert call(**{k: NUL}) == 1, k
+    assert call(B=-1) == 2
+    assert call(topk=0) == 2
+    assert call(B=1 << 16, S=1 << 16) == 2  # B*S beyond int32
+    assert call(D=576) == 3
+    assert call(H=65) == 3
+    assert call(r=1) == 3
+    assert call(wr=1) == 3
+    assert call(q=C.c_void_p(0x1002)) == 3
+    assert call(wsb=need - 1) == 4
+    assert call(ws=C.c_void_p(0x10010)) == 4  # misaligned
+    assert call(ws=NUL) == 4
+    assert call(S=0) == 0  # nothing to do
+    # indexer
+    inames = ["q", "k", "w", "su", "B", "S", "Sc", "Hi", "Di", "r", "topk", "idx", "val", "ws",
+              "wsb", "stream"]
+    ineed = L.csa_bsnd_indexer_workspace_size(3, 200, 50, 8, 64, 16)
+    assert ineed > 0
+    ibase = dict(q=P, k=P, w=P, su=NUL, B=3, S=200, Sc=50, Hi=8, Di=64, r=4, topk=16, idx=P,
+                 val=NUL, ws=C.c_void_p(0x10000), wsb=ineed, stream=NUL)
+
+    def icall(**kw):
+        a = dict(ibase)
+        a.update(kw)
+        return L.csa_indexer_topk_bsnd(*[a[n] for n in inames])
+
+    for k in ("q", "k", "w", "idx"):
+        assert icall(**{k: NUL}) == 1, k
+    assert icall(topk=0) == 2
+    assert icall(Sc=-1) == 2
+    assert icall(Di=96) == 3
+    assert icall(Hi=65) == 3
+    assert icall(r=1) == 3
+    assert icall(wsb=ineed - 1) == 4
+    assert icall(B=0) == 0
+
+
 def test_product_does_not_import_oracle():
     pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
     for dirpath, _, files in os.walk(pkg):
