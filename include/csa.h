@@ -1,8 +1,9 @@
 /*
  * csa.h -- C ABI of the GB300 (sm_103a) forward path of DeepSeek-V4
  * Compressed Sparse Attention (CSA) and its compressor-only mode (HCA) over
- * THD-packed variable-length sequences, on one GPU, and of the backward of
- * its sparse MLA attention.
+ * THD-packed variable-length sequences (and fixed-shape BSND batches), on one
+ * GPU, of the backward of its sparse MLA attention and of the indexer's
+ * KL-loss gradient.
  *
  * Sources (web pages, cited by title and section):
  *   [miles#2038]  "PR #2038 完整报告" (radixark/miles): "Enable THD

@@ -1,5 +1,6 @@
-"""GB300 (sm_103a) forward path of DeepSeek-V4 Compressed Sparse Attention,
-and the backward of its sparse MLA attention.
+"""GB300 (sm_103a) forward path of DeepSeek-V4 Compressed Sparse Attention
+(THD, and BSND batches), the backward of its sparse MLA attention and the
+indexer's KL-loss gradient.
 
 Thin Python binding of the C ABI declared in ``include/csa.h`` (same call
 names). It only marshals arguments: every step of the path runs in the CUDA
