@@ -26,10 +26,12 @@
 // floats so that each quarter-warp's float4 reads hit 32 distinct banks).
 // Pass 1 computes a and I chunk by chunk; pass 2 recomputes a with the same
 // code (identical fp32 values, hence identical ReLU decisions), then
-// accumulates d_w (one head per thread), d_q (32 or 16 outputs per thread in
-// registers) and the chunk's row gradients, which are added to d_k with
-// 16-byte atomics (a warp covers 512 contiguous bytes of one row). All
-// arithmetic is fp32 on the CUDA cores.
+// accumulates d_w (one head per thread), d_q (a 4-head x 8- or 4-column
+// register tile per thread) and the chunk's row gradients (4 or 2 rows x 4
+// columns per thread), which are added to d_k with 16-byte atomics (a warp
+// covers 512 contiguous bytes of one row). Every contraction reads its
+// shared operands as float4 register tiles, about one load per 5-10 FMAs.
+// All arithmetic is fp32 on the CUDA cores.
 #include "common.cuh"
 #include "internal.h"
 
@@ -45,13 +47,15 @@ constexpr int kKlWarps = kKlThreads / 32;
 
 template <int DI>
 struct KlSmem {
-    float q[kKlHeads][DI];             // the token's q, fp32 (rows >= Hi zero)
+    float q[kKlHeads][DI + 4];         // the token's q, fp32 (rows >= Hi zero)
     float k[kKlChunk][DI + 4];         // a chunk of k rows, fp32
-    float a[kKlHeads][kKlChunk + 1];   // a_hs of the chunk, then the coefficients G
+    float a[kKlHeads][kKlChunk + 1];   // a_hs of the chunk
+    float g[kKlHeads][kKlChunk + 4];   // G[h][c] = g_c w_h [a_hc > 0]
+    float gt[kKlChunk][kKlHeads + 4];  // the same, transposed
     float w[kKlHeads];
     int32_t rows[kKlMaxList];          // the token's valid rows, in list order
     float p[kKlMaxList];               // their targets (unnormalised)
-    float g[kKlMaxList];               // scores I, then dL/dI
+    float dl[kKlMaxList];              // scores I, then dL/dI
     float red[kKlWarps + 1];
     int32_t scan[kKlWarps + 1];
     int32_t info[4];                   // segment, cu_q[b], cu_c[b], cu_c[b+1]
@@ -110,29 +114,40 @@ __device__ __forceinline__ void load_k_chunk(KlSmem<DI> &s, const __nv_bfloat16 
     }
 }
 
-// a[h][c] = q[h,:] . k[c,:] for the 64 heads x 32 rows of a chunk: lane c,
-// heads warp + 8 i. Pass 1 and pass 2 run this same code, so their fp32
-// values (and ReLU decisions) are identical.
+// a[h][c] = q[h,:] . k[c,:] for the 64 heads x 32 rows of a chunk. Thread
+// tile: heads 4 hb .. 4 hb + 3 and rows cb, cb + 16 (hb = tid / 16,
+// cb = tid % 16). Per 4 dims it reads 4 + 2 float4 for 32 FMAs; a
+// quarter-warp's k rows are 132 floats apart (distinct banks) and the two
+// head blocks of a warp are 4 padded rows apart (distinct banks). Pass 1 and
+// pass 2 run this same code, so their fp32 values (and ReLU decisions) are
+// identical.
 template <int DI>
 __device__ __forceinline__ void chunk_dots(KlSmem<DI> &s) {
-    const int c = threadIdx.x & 31, hg = threadIdx.x >> 5;
-    float acc[kKlHeads / kKlWarps];
+    const int hb = threadIdx.x >> 4, cb = threadIdx.x & 15;
+    float acc[4][2];
 #pragma unroll
-    for (int i = 0; i < kKlHeads / kKlWarps; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.0f;
 #pragma unroll 4
     for (int d = 0; d < DI; d += 4) {
-        const float4 kv = *reinterpret_cast<const float4 *>(&s.k[c][d]);
+        float4 kv[2], qv[4];
 #pragma unroll
-        for (int i = 0; i < kKlHeads / kKlWarps; ++i) {
-            const float4 qv = *reinterpret_cast<const float4 *>(&s.q[hg + kKlWarps * i][d]);
-            acc[i] = fmaf(qv.x, kv.x, acc[i]);
-            acc[i] = fmaf(qv.y, kv.y, acc[i]);
-            acc[i] = fmaf(qv.z, kv.z, acc[i]);
-            acc[i] = fmaf(qv.w, kv.w, acc[i]);
-        }
+        for (int j = 0; j < 2; ++j) kv[j] = *reinterpret_cast<const float4 *>(&s.k[cb + 16 * j][d]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4 *>(&s.q[4 * hb + i][d]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                acc[i][j] = fmaf(qv[i].x, kv[j].x, acc[i][j]);
+                acc[i][j] = fmaf(qv[i].y, kv[j].y, acc[i][j]);
+                acc[i][j] = fmaf(qv[i].z, kv[j].z, acc[i][j]);
+                acc[i][j] = fmaf(qv[i].w, kv[j].w, acc[i][j]);
+            }
     }
 #pragma unroll
-    for (int i = 0; i < kKlHeads / kKlWarps; ++i) s.a[hg + kKlWarps * i][c] = acc[i];
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) s.a[4 * hb + i][cb + 16 * j] = acc[i][j];
 }
 
 template <int DI>
@@ -141,10 +156,14 @@ __global__ void __launch_bounds__(kKlThreads, 2) indexer_kl_grad_kernel(IndexerK
     KlSmem<DI> &s = *reinterpret_cast<KlSmem<DI> *>(smem_raw);
     const IndexerKlArgs &a = args;
     const int tid = threadIdx.x;
-    constexpr int kGroups = kKlThreads / DI;         // head groups of the d_q mapping
-    constexpr int kDq = kKlHeads / kGroups;           // d_q accumulators per thread
-    constexpr int kQuads = DI / 4;                    // float4 columns of a row
-    constexpr int kRowsPerPass = kKlThreads / kQuads; // rows of the d_k mapping per pass
+    // d_q tile: heads 4 hb .. 4 hb + 3 x columns 64 gi + 4 db + e (hb = tid / 16,
+    // db = tid % 16, gi < DI / 64, e < 4)
+    constexpr int kQg = DI / 64;
+    // d_k tile: rows kKr cb .. kKr cb + kKr - 1 x columns 4 db .. 4 db + 3
+    // (db = tid % (DI / 4), cb = tid / (DI / 4))
+    constexpr int kQuads = DI / 4;
+    constexpr int kKr = kKlChunk * kQuads / kKlThreads;  // 4 (Di 128) or 2 (Di 64)
+    static_assert(kKr == 2 || kKr == 4, "d_k tile");
 
     for (int32_t t = blockIdx.x; t < a.T; t += gridDim.x) {
         // ---- the token's segment, q and w ----
@@ -236,36 +255,38 @@ __global__ void __launch_bounds__(kKlThreads, 2) indexer_kl_grad_kernel(IndexerK
             if (tid < kKlChunk && c0 + tid < n) {
                 float sc = 0.0f;
                 for (int h = 0; h < a.Hi; ++h) sc = fmaf(s.w[h], fmaxf(s.a[h][tid], 0.0f), sc);
-                s.g[c0 + tid] = sc;
+                s.dl[c0 + tid] = sc;
             }
             __syncthreads();
         }
 
         // ---- log-softmax over the entries, loss, dL/dI ----
         float mx = -INFINITY;
-        for (int i = tid; i < n; i += kKlThreads) mx = fmaxf(mx, s.g[i]);
+        for (int i = tid; i < n; i += kKlThreads) mx = fmaxf(mx, s.dl[i]);
         mx = block_max(mx, s.red);
         float z = 0.0f;
-        for (int i = tid; i < n; i += kKlThreads) z += expf(s.g[i] - mx);
+        for (int i = tid; i < n; i += kKlThreads) z += expf(s.dl[i] - mx);
         z = block_sum(z, s.red);
         const float lz = mx + logf(z);
         float kl = 0.0f;
         for (int i = tid; i < n; i += kKlThreads) {
             const float ps = s.p[i] * inv_mass;
-            const float log_pi = s.g[i] - lz;
+            const float log_pi = s.dl[i] - lz;
             if (ps > 0.0f) kl += ps * (logf(ps) - log_pi);
-            s.g[i] = a.grad_scale * (expf(log_pi) - ps);
+            s.dl[i] = a.grad_scale * (expf(log_pi) - ps);
         }
         kl = block_sum(kl, s.red);  // also orders the g writes before their reads
         if (tid == 0 && a.loss) a.loss[t] = kl;
 
         // ---- pass 2: gradients ----
-        float dq[kDq];
+        float dq[4][4 * kQg];
 #pragma unroll
-        for (int i = 0; i < kDq; ++i) dq[i] = 0.0f;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 4 * kQg; ++e) dq[i][e] = 0.0f;
         float dw = 0.0f;
-        const int dq_d = tid % DI, dq_h0 = tid / DI;
-        const int dk_d = (tid % kQuads) * 4, dk_r0 = tid / kQuads;
+        const int q_hb = tid >> 4, q_db = tid & 15;
+        const int k_db = tid % kQuads, k_cb = tid / kQuads;
         for (int c0 = 0; c0 < n; c0 += kKlChunk) {
             load_k_chunk(s, a.k, c0, n);
             __syncthreads();
@@ -273,43 +294,74 @@ __global__ void __launch_bounds__(kKlThreads, 2) indexer_kl_grad_kernel(IndexerK
             __syncthreads();
             const int nc = min(kKlChunk, n - c0);
             if (tid < kKlHeads)
-                for (int c = 0; c < nc; ++c) dw = fmaf(s.g[c0 + c], fmaxf(s.a[tid][c], 0.0f), dw);
-            __syncthreads();
-            // G[h][c] = g_c w_h [a_hc > 0] (zero past the chunk's rows)
+                for (int c = 0; c < nc; ++c) dw = fmaf(s.dl[c0 + c], fmaxf(s.a[tid][c], 0.0f), dw);
+            // G[h][c] = g_c w_h [a_hc > 0] (zero past the chunk's rows), and its transpose
             for (int e = tid; e < kKlHeads * kKlChunk; e += kKlThreads) {
                 const int h = e / kKlChunk, c = e % kKlChunk;
-                const float av = s.a[h][c];
-                s.a[h][c] = (c < nc && av > 0.0f) ? s.g[c0 + c] * s.w[h] : 0.0f;
+                const float gv = (c < nc && s.a[h][c] > 0.0f) ? s.dl[c0 + c] * s.w[h] : 0.0f;
+                s.g[h][c] = gv;
+                s.gt[c][h] = gv;
             }
             __syncthreads();
-            // d_q[h][d] += sum_c G[h][c] k[c][d]
+            // d_q[h][d] += sum_c G[h][c] k[c][d]: 3 (Di 128) or 2 float4 reads per 32 or 16 FMAs
 #pragma unroll 4
             for (int c = 0; c < kKlChunk; ++c) {
-                const float kv = s.k[c][dq_d];
+                const float4 gv = *reinterpret_cast<const float4 *>(&s.gt[c][4 * q_hb]);
+                const float gh[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-                for (int i = 0; i < kDq; ++i) dq[i] = fmaf(s.a[dq_h0 + kGroups * i][c], kv, dq[i]);
-            }
-            // d_k[row c][d..d+3] += sum_h G[h][c] q[h][d..d+3]
+                for (int gi = 0; gi < kQg; ++gi) {
+                    const float4 kv = *reinterpret_cast<const float4 *>(&s.k[c][64 * gi + 4 * q_db]);
 #pragma unroll
-            for (int r = dk_r0; r < kKlChunk; r += kRowsPerPass) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int h = 0; h < a.Hi; ++h) {
-                    const float gv = s.a[h][r];
-                    const float4 qv = *reinterpret_cast<const float4 *>(&s.q[h][dk_d]);
-                    acc.x = fmaf(gv, qv.x, acc.x);
-                    acc.y = fmaf(gv, qv.y, acc.y);
-                    acc.z = fmaf(gv, qv.z, acc.z);
-                    acc.w = fmaf(gv, qv.w, acc.w);
+                    for (int i = 0; i < 4; ++i) {
+                        dq[i][4 * gi + 0] = fmaf(gh[i], kv.x, dq[i][4 * gi + 0]);
+                        dq[i][4 * gi + 1] = fmaf(gh[i], kv.y, dq[i][4 * gi + 1]);
+                        dq[i][4 * gi + 2] = fmaf(gh[i], kv.z, dq[i][4 * gi + 2]);
+                        dq[i][4 * gi + 3] = fmaf(gh[i], kv.w, dq[i][4 * gi + 3]);
+                    }
                 }
-                if (r < nc)
-                    atomicAdd(reinterpret_cast<float4 *>(a.d_k + (int64_t)s.rows[c0 + r] * DI + dk_d), acc);
+            }
+            // d_k[row c][d..d+3] += sum_h G[h][c] q[h][d..d+3] for kKr rows per thread
+            {
+                float4 acc[kKr];
+#pragma unroll
+                for (int r = 0; r < kKr; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int h = 0; h < a.Hi; ++h) {
+                    float gr[kKr];
+                    if constexpr (kKr == 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(&s.g[h][4 * k_cb]);
+                        gr[0] = v.x, gr[1] = v.y, gr[2] = v.z, gr[3] = v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2 *>(&s.g[h][2 * k_cb]);
+                        gr[0] = v.x, gr[1] = v.y;
+                    }
+                    const float4 qv = *reinterpret_cast<const float4 *>(&s.q[h][4 * k_db]);
+#pragma unroll
+                    for (int r = 0; r < kKr; ++r) {
+                        acc[r].x = fmaf(gr[r], qv.x, acc[r].x);
+                        acc[r].y = fmaf(gr[r], qv.y, acc[r].y);
+                        acc[r].z = fmaf(gr[r], qv.z, acc[r].z);
+                        acc[r].w = fmaf(gr[r], qv.w, acc[r].w);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kKr; ++r) {
+                    const int c = kKr * k_cb + r;
+                    if (c < nc)
+                        atomicAdd(reinterpret_cast<float4 *>(a.d_k + (int64_t)s.rows[c0 + c] * DI +
+                                                             4 * k_db),
+                                  acc[r]);
+                }
             }
             __syncthreads();  // the chunk's k rows and coefficients are rewritten next
         }
 #pragma unroll
-        for (int i = 0; i < kDq; ++i) {
-            const int h = dq_h0 + kGroups * i;
-            if (h < a.Hi) dq_out[h * DI + dq_d] = dq[i];
+        for (int i = 0; i < 4; ++i) {
+            const int h = 4 * q_hb + i;
+            if (h < a.Hi)
+#pragma unroll
+                for (int gi = 0; gi < kQg; ++gi)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dq_out[h * DI + 64 * gi + 4 * q_db + e] = dq[i][4 * gi + e];
         }
         if (tid < a.Hi) a.d_w[(int64_t)t * a.Hi + tid] = dw;
         __syncthreads();  // shared q, w and lists are rewritten by the next token
