@@ -44,9 +44,11 @@ def lib():
         _lib.csa_ref_indexer_kl_loss_grad.argtypes = [
             f64p, f64p, f64p, i32p, f64p, i32, i32, i32, i32, i32, i32p, i32p, i32, i32,
             C.c_double, i32p, i32, f64p, f64p, f64p, f64p, f64p]
+        _lib.csa_ref_compress_thd.argtypes = [
+            f64p, f64p, f64p, i32p, i32p, i32, i32, i32, i32, i32, f64p]
         for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx",
                      "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd",
-                     "csa_ref_indexer_kl_loss_grad"):
+                     "csa_ref_indexer_kl_loss_grad", "csa_ref_compress_thd"):
             getattr(_lib, name).restype = C.c_int
     return _lib
 
@@ -219,3 +221,20 @@ def indexer_kl_loss_grad(q_rows, k, w_rows, sparse_indices, attn_l1, total_token
         _p(res["d_q"], C.c_double), _p(res["d_k"], C.c_double), _p(res["d_w"], C.c_double),
         _p(res["loss"], C.c_double), _p(res["g"], C.c_double)), "indexer_kl_loss_grad")
     return res
+
+
+def compress_thd(kv, score, ape, cu_seqlens, cmp_ratio: int, head_dim: int, overlap: bool):
+    """THD compressor core in fp64: grouping, ape, overlap transform and
+    softmax pooling over the slots. kv/score [T, Wd] (Wd = 2 head_dim with
+    overlap), ape [cmp_ratio, Wd] or None. Returns [Tc, head_dim]."""
+    k = _f64(kv)
+    s = _f64(score)
+    a = _f64(ape)
+    cu = _i32(cu_seqlens)
+    cuc = compress_cu_seqlens(cu, cmp_ratio)
+    out = np.zeros((int(cuc[-1]), head_dim))
+    _check(lib().csa_ref_compress_thd(
+        _p(k, C.c_double), _p(s, C.c_double), _p(a, C.c_double), _p(cu, C.c_int32),
+        _p(cuc, C.c_int32), len(cu) - 1, int(cu[-1]), cmp_ratio, head_dim, 1 if overlap else 0,
+        _p(out, C.c_double)), "compress_thd")
+    return out

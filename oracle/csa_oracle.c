@@ -15,7 +15,8 @@
  *     rows, with a per-head attention sink;
  *   - its backward: gradients of q, of both KV streams and of the sinks,
  *     and the head-averaged attention distributions;
- *   - the indexer's KL loss against that distribution, and its gradients.
+ *   - the indexer's KL loss against that distribution, and its gradients;
+ *   - the THD compressor's grouping, overlap transform and slot pooling.
  * Every floating-point input arrives as double (bf16 inputs are widened
  * exactly by the caller); every sum, exp and log is done in double.
  *
@@ -641,6 +642,96 @@ int csa_ref_indexer_kl_loss_grad(const double *q, const double *k, const double 
             }
         }
         free(rows), free(slot), free(score), free(p), free(dots), free(gk);
+    }
+    return err;
+}
+
+/*
+ * THD compressor: grouping, overlap transform and pooling of one compressor
+ * (miles PR 2038 report, compressor.py DeepSeekV4Compressor._forward_thd and
+ * _overlap_transform_thd).
+ *
+ * Inputs are the two projections of the packed rows, kv = x W_kv^T and
+ * score = x W_gate^T ([T, Wd] fp32, Wd = 2 head_dim with overlap, head_dim
+ * without; the page computes them with linear_bf16_fp32), and the absolute
+ * position embedding ape [cmp_ratio, Wd] (may be NULL: zero).
+ * Grouping (gather_idx): compressed row g = cu_c[b] + j of sequence b takes
+ * the rows cu[b] + j r + i, i < r, of kv and score; ape[i] is added to the
+ * score of slot i (reading: the page shows ape viewed as [1, ratio, 1, -1]
+ * next to the grouped tensors and omits where it is added).
+ * Overlap (when overlap != 0): each group becomes 2r slots of head_dim: slot
+ * i < r holds the first half (columns [0, hd)) of row i of the previous
+ * group of the same sequence, slot r + i the second half (columns [hd, 2hd))
+ * of its own row i; the first group of a sequence has no predecessor, and
+ * its slots i < r are filled with 0 (kv) and -inf (score).
+ * Pooling (reading: the page omits everything after the overlap transform;
+ * the -inf fill of the score only has a meaning as a softmax logit): per
+ * compressed row and dimension e,
+ *     out[g, e] = sum_s softmax_s(score[g, s, e]) kv[g, s, e]
+ * over the group's slots. out is [Tc, head_dim], fp64 here.
+ * Returns REF_ERR_ARG on inconsistent arguments.
+ */
+int csa_ref_compress_thd(const double *kv, const double *score, const double *ape,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp, int32_t batch,
+                         int32_t T, int32_t cmp_ratio, int32_t head_dim, int32_t overlap,
+                         double *out) {
+    if (!kv || !score || !cu_seqlens || !cu_seqlens_cmp || !out) return REF_ERR_ARG;
+    if (T < 0 || cmp_ratio < 1 || head_dim < 1 || batch < 0) return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, T)) return REF_ERR_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+        int32_t len = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (cu_seqlens_cmp[b + 1] - cu_seqlens_cmp[b] != len / cmp_ratio) return REF_ERR_ARG;
+    }
+    if (cu_seqlens_cmp[0] != 0) return REF_ERR_ARG;
+    const int32_t r = cmp_ratio, hd = head_dim;
+    const int32_t wd = overlap ? 2 * hd : hd;
+    const int32_t slots = overlap ? 2 * r : r;
+    const int32_t Tc = cu_seqlens_cmp[batch];
+    int err = REF_OK;
+#pragma omp parallel for schedule(static)
+    for (int32_t g = 0; g < Tc; ++g) {
+        int32_t b = segment_of(cu_seqlens_cmp, batch, g);
+        int32_t j = g - cu_seqlens_cmp[b];
+        double *sk = (double *)malloc(sizeof(double) * (size_t)slots);
+        double *sv = (double *)malloc(sizeof(double) * (size_t)slots);
+        if (!sk || !sv) {
+            free(sk), free(sv);
+            err = REF_ERR_NOMEM;
+            continue;
+        }
+        for (int32_t e = 0; e < hd; ++e) {
+            /* the group's slots for dimension e, after grouping, ape and overlap */
+            for (int32_t i = 0; i < r; ++i) {
+                int64_t own = cu_seqlens[b] + (int64_t)j * r + i;
+                if (overlap) {
+                    if (j == 0) {
+                        sv[i] = 0.0;
+                        sk[i] = -INFINITY;
+                    } else {
+                        int64_t prev = own - r;
+                        sv[i] = kv[prev * wd + e];
+                        sk[i] = score[prev * wd + e] + (ape ? ape[(int64_t)i * wd + e] : 0.0);
+                    }
+                    sv[r + i] = kv[own * wd + hd + e];
+                    sk[r + i] = score[own * wd + hd + e] + (ape ? ape[(int64_t)i * wd + hd + e] : 0.0);
+                } else {
+                    sv[i] = kv[own * wd + e];
+                    sk[i] = score[own * wd + e] + (ape ? ape[(int64_t)i * wd + e] : 0.0);
+                }
+            }
+            double m = -INFINITY;
+            for (int32_t s = 0; s < slots; ++s)
+                if (sk[s] > m) m = sk[s];
+            double z = 0.0, acc = 0.0;
+            for (int32_t s = 0; s < slots; ++s) {
+                if (sk[s] == -INFINITY) continue;
+                double p = exp(sk[s] - m);
+                z += p;
+                acc += p * sv[s];
+            }
+            out[(int64_t)g * hd + e] = acc / z;
+        }
+        free(sk), free(sv);
     }
     return err;
 }
