@@ -29,6 +29,8 @@ MLA backward of every layer, timed per launch from the forward's out and
 lse, with its FLOPs against the bf16 tensor peak. ``--kl`` adds one more: the
 indexer KL-loss gradient of the indexer layer, on its own top-k rows with
 the attention backward's distribution as target, against the fp32 ALU peak.
+``--cmp`` adds the THD compressor core (grouping, overlap, slot pooling) for
+each layer's ratio, against the measured HBM bandwidth.
 """
 
 from __future__ import annotations
@@ -74,6 +76,9 @@ def parse_args():
                    help="also time the sparse MLA backward of every layer and print its own "
                         "JSON line after the forward's (off by default: one line per run)")
     p.add_argument("--bwd-steps", type=int, default=5)
+    p.add_argument("--cmp", action="store_true",
+                   help="also time the THD compressor core for each layer's ratio "
+                        "(one more JSON line)")
     p.add_argument("--kl", action="store_true",
                    help="also time the indexer KL-loss gradient of each indexer layer "
                         "(one more JSON line)")
@@ -476,7 +481,67 @@ def run_ours(args, world, rank, local):
         result["_bwd"] = run_bwd(args, layers, stream, flush, peaks, peak_kind)
     if args.kl and rank == 0:
         result["_kl"] = run_kl(args, layers, stream, flush)
+    if args.cmp and rank == 0:
+        result["_cmp"] = run_cmp(args, layers, stream, flush, peaks, peak_kind)
     return result
+
+
+def run_cmp(args, layers, stream, flush, peaks, peak_src):
+    """The THD compressor core for each layer's ratio on this pack (head_dim
+    512, overlap, position embedding), from seeded N(0,1) projections drawn
+    on the device, timed per launch with CUDA events between L2 flushes.
+    Algorithmic bytes: every grouped row of both projections read once
+    (2 x 1024 fp32 each), the position embedding and the fp32 output."""
+    import sparse_attention_csa_gb300 as csa
+    spec = layers[0].spec
+    T, hd = spec.total_tokens, 512
+    dev = layers[0].cu.device
+    gen = torch.Generator(device=dev).manual_seed(9)
+    kv = torch.randn((T, 2 * hd), generator=gen, device=dev)
+    score = torch.randn((T, 2 * hd), generator=gen, device=dev)
+    per, nbytes = {}, 0
+    for L in layers:
+        r = L.layer.cmp_ratio
+        ape = torch.randn((r, 2 * hd), generator=gen, device=dev)
+        out = torch.empty((L.Tc, hd), dtype=torch.float32, device=dev)
+
+        def call():
+            return csa.csa_compress_thd(kv, score, ape, L.cu, L.cuc, L.Tc, r, hd, True, out=out,
+                                        stream=stream)
+
+        csa.csa_compress_cu_seqlens(L.cu, r, out=L.cuc, stream=stream)
+        for _ in range(3):
+            flush.zero_()
+            call()
+        ms = []
+        for _ in range(max(args.bwd_steps, 5)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        per[f"compress_thd/r{r}"] = statistics.median(ms)
+        grouped = L.Tc * r
+        nbytes += 2 * grouped * 2 * hd * 4 + r * 2 * hd * 4 + L.Tc * hd * 4
+    st, word = csa.csa_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the compressor: {word:#x}")
+    total = sum(per.values())
+    achieved = nbytes / (total * 1e-3) / 1e9
+    return {
+        "metric": "THD compressor core tokens/s (grouping, overlap, slot softmax pooling) on 1 GB300",
+        "value": T * len(layers) / (total * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": max(args.bwd_steps, 5), "warmup": 3, "ms_per_step": total,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic", "part": "compressor",
+        "config": {"workload": f"{spec.name}, one compressor per layer ratio, head_dim 512, "
+                               "overlap, projections given", "l2": "flushed between launches"},
+        "kernels_ms": per,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": peak_src, "bytes": nbytes},
+    }
 
 
 def fp32_alu_peak_tflops():
@@ -712,9 +777,10 @@ def main():
     res = run_ours(args, world, rank, local)
     bwd = res.pop("_bwd", None)
     kl = res.pop("_kl", None)
+    cmp_line = res.pop("_cmp", None)
     if rank == 0:
         print(json.dumps(res), flush=True)
-        for extra in (bwd, kl):
+        for extra in (bwd, kl, cmp_line):
             if extra is not None:
                 print(json.dumps(extra), flush=True)
     if world > 1:

@@ -217,3 +217,9 @@ def draw_uniform(shape, seed: int, low: float = 0.0, high: float = 1.0) -> torch
     """fp32 U(low, high) tensor (CPU) from a generator seeded with ``seed``."""
     gen = torch.Generator("cpu").manual_seed(seed)
     return low + (high - low) * _rand(gen, tuple(shape))
+
+
+def draw_normal(shape, seed: int) -> torch.Tensor:
+    """fp32 N(0,1) tensor (CPU) from a generator seeded with ``seed``."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return _randn(gen, tuple(shape), torch.float32)

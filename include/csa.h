@@ -281,6 +281,37 @@ csa_status_t csa_indexer_kl_loss_grad(const csa_bf16_t *q, const csa_bf16_t *k, 
                                       csa_stream_t stream);
 
 /*
+ * THD compressor core: grouping, position embedding, overlap transform and
+ * slot pooling of one DeepSeek-V4 compressor, producing the compressed rows
+ * (cmp_kv, or the indexer's k) from the two projections of the packed rows.
+ * [miles#2038] 关键源码片段 compressor.py (_forward_thd: per-sequence groups
+ * of cmp_ratio rows, gather_idx, the len % cmp_ratio tail produces no row;
+ * _overlap_transform_thd: [Tc, r, 2hd] -> [Tc, 2r, hd], the first r slots
+ * from the previous group's first halves, a sequence's first group filled
+ * with 0 for kv and -inf for the score). The page omits the rest; reading:
+ * ape[i] is added to slot i's score before the overlap, and
+ *     out[g, e] = sum_s softmax_s(score[g, s, e]) kv[g, s, e]
+ * over the group's slots (r, or 2r with overlap). The linear projections
+ * (linear_bf16_fp32 on the page) and any later normalisation or RoPE are the
+ * caller's.
+ * kv, score [T, Wd] fp32 (Wd = 2 * head_dim with overlap, head_dim without);
+ * ape [cmp_ratio, Wd] fp32 or NULL (zero); cu_seqlens, cu_seqlens_cmp
+ * [batch+1] int32 (the latter from csa_compress_cu_seqlens); out
+ * [total_cmp, head_dim] fp32, overwritten.
+ * Errors: negative sizes, head_dim < 1 or total_cmp * cmp_ratio >
+ * total_tokens -> CSA_ERR_SHAPE; cmp_ratio < 1 or head_dim > 65536 ->
+ * CSA_ERR_UNSUPPORTED; NULL kv/score/cu_seqlens/cu_seqlens_cmp/out ->
+ * CSA_ERR_NULL. total_cmp == 0 launches nothing. A compressed row whose
+ * group does not fit inside its sequence (inconsistent device offsets) is
+ * written as 0 and recorded in the device error word.
+ */
+csa_status_t csa_compress_thd(const float *kv, const float *score, const float *ape,
+                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp,
+                              int32_t batch, int32_t total_tokens, int32_t total_cmp,
+                              int32_t cmp_ratio, int32_t head_dim, int32_t overlap, float *out,
+                              csa_stream_t stream);
+
+/*
  * BSND layout (fixed-shape batch) of the forward path.
  * [hp#RFC] sections 1 and 2: the ops take a layout argument whose default is
  * "BSND" -- q [B, S, N, D], KV [B, S_kv, 1, D], compressed indices local to

@@ -24,7 +24,8 @@ __all__ = [
     "csa_window_idx", "csa_indexer_topk_workspace_size", "csa_indexer_topk",
     "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
     "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
-    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "EXPORTED_SYMBOLS",
+    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "csa_compress_thd",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "csa_indexer_topk_workspace_size", "csa_indexer_topk", "csa_sparse_mla_fwd",
     "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
     "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
-    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd",
+    "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "csa_compress_thd",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -92,10 +93,12 @@ def lib():
         L.csa_bsnd_indexer_workspace_size.argtypes = [_i32] * 6
         L.csa_indexer_topk_bsnd.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                             _i32, _i32, _vp, _vp, _vp, _sz, _vp]
+        L.csa_compress_thd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                       _i32, _vp, _vp]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
                      "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error",
                      "csa_indexer_topk_noalloc", "csa_indexer_kl_loss_grad",
-                     "csa_sparse_mla_fwd_bsnd", "csa_indexer_topk_bsnd"):
+                     "csa_sparse_mla_fwd_bsnd", "csa_indexer_topk_bsnd", "csa_compress_thd"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -401,6 +404,30 @@ def csa_indexer_topk_bsnd(q, k, w, seqused, cmp_ratio: int, topk: int,
         int(cmp_ratio), int(topk), _ptr(out), _ptr(out_val) if return_value else None,
         _ptr(workspace), ws_bytes, _stream(stream)), "csa_indexer_topk_bsnd")
     return out, (out_val if return_value else None)
+
+
+def csa_compress_thd(kv, score, ape, cu_seqlens, cu_seqlens_cmp, total_cmp: int,
+                     cmp_ratio: int, head_dim: int, overlap: bool = True, out=None, stream=None):
+    """Compressed rows [total_cmp, head_dim] fp32 from the projections kv and
+    score [T, Wd] fp32 (Wd = 2 head_dim with overlap) and ape [cmp_ratio, Wd]
+    or None: per-sequence groups, overlap transform, softmax pooling over
+    the slots. ``total_cmp`` is cu_seqlens_cmp's last entry (a host int)."""
+    _need(kv, "kv", torch.float32, 2)
+    _need(score, "score", torch.float32, 2)
+    _need(ape, "ape", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(cu_seqlens_cmp, "cu_seqlens_cmp", torch.int32, 1)
+    T, wd = kv.shape
+    if tuple(score.shape) != (T, wd) or wd != (2 * head_dim if overlap else head_dim):
+        raise ValueError("kv and score must both be [T, 2*head_dim] (overlap) or [T, head_dim]")
+    if out is None:
+        out = torch.empty((total_cmp, head_dim), dtype=torch.float32, device=kv.device)
+    _need(out, "out", torch.float32, 2)
+    _check(lib().csa_compress_thd(
+        _ptr(kv), _ptr(score), _ptr(ape), _ptr(cu_seqlens), _ptr(cu_seqlens_cmp),
+        cu_seqlens.numel() - 1, T, int(total_cmp), int(cmp_ratio), int(head_dim),
+        1 if overlap else 0, _ptr(out), _stream(stream)), "csa_compress_thd")
+    return out
 
 
 def csa_device_error(stream=None):

@@ -24,6 +24,7 @@ enum KernelId : int32_t {
     kKerMlaBwd = 5,
     kKerIndexerKl = 6,
     kKerBsnd = 7,
+    kKerCompressor = 8,
 };
 
 __device__ __forceinline__ void report_error(int32_t *err, int32_t kind, int32_t kernel,

@@ -302,6 +302,36 @@ csa_status_t csa_indexer_kl_loss_grad(const csa_bf16_t *q, const csa_bf16_t *k, 
     return from_cuda(csa::launch_indexer_kl_grad(a, (cudaStream_t)stream));
 }
 
+csa_status_t csa_compress_thd(const float *kv, const float *score, const float *ape,
+                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_cmp,
+                              int32_t batch, int32_t total_tokens, int32_t total_cmp,
+                              int32_t cmp_ratio, int32_t head_dim, int32_t overlap, float *out,
+                              csa_stream_t stream) {
+    if (batch < 0 || total_tokens < 0 || total_cmp < 0 || head_dim < 1) return CSA_ERR_SHAPE;
+    if ((int64_t)total_cmp * cmp_ratio > total_tokens) return CSA_ERR_SHAPE;
+    if (cmp_ratio < 1 || head_dim > 65536) return CSA_ERR_UNSUPPORTED;
+    if (total_cmp == 0) return CSA_OK;  // nothing to pool (empty buffers may be NULL)
+    if (!kv || !score || !cu_seqlens || !cu_seqlens_cmp || !out) return CSA_ERR_NULL;
+    csa_status_t st;
+    int32_t *err = error_word(&st);
+    if (st != CSA_OK) return st;
+    csa::CompressArgs a;
+    a.kv = kv;
+    a.score = score;
+    a.ape = ape;
+    a.cu_q = cu_seqlens;
+    a.cu_c = cu_seqlens_cmp;
+    a.out = out;
+    a.err = err;
+    a.T = total_tokens;
+    a.Tc = total_cmp;
+    a.batch = batch;
+    a.r = cmp_ratio;
+    a.hd = head_dim;
+    a.overlap = overlap ? 1 : 0;
+    return from_cuda(csa::launch_compress_thd(a, (cudaStream_t)stream));
+}
+
 csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail) {
     csa_status_t st;
     int32_t *err = error_word(&st);

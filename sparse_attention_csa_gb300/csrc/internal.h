@@ -104,6 +104,19 @@ cudaError_t launch_indexer_kl_grad(const IndexerKlArgs &a, cudaStream_t stream);
 // Largest topk (entries of sparse_indices per token) the kernel accepts.
 int32_t indexer_kl_max_topk();
 
+struct CompressArgs {
+    const float *kv;      // [T, wd] (wd = 2 hd with overlap, hd without)
+    const float *score;   // [T, wd]
+    const float *ape;     // [r, wd] or nullptr
+    const int32_t *cu_q;  // [batch+1]
+    const int32_t *cu_c;  // [batch+1]
+    float *out;           // [Tc, hd]
+    int32_t *err;
+    int32_t T, Tc, batch, r, hd, overlap;
+};
+
+cudaError_t launch_compress_thd(const CompressArgs &a, cudaStream_t stream);
+
 // Device error word of the current device (csa_api.cu).
 int32_t *device_error_word(csa_status_t *st);
 

@@ -225,6 +225,27 @@ def test_bsnd_rejects(L):
     assert icall(B=0) == 0
 
 
+def test_compress_thd_rejects(L):
+    names = ["kv", "score", "ape", "cu", "cuc", "batch", "T", "Tc", "r", "hd", "ov", "out",
+             "stream"]
+    base = dict(kv=P, score=P, ape=NUL, cu=P, cuc=P, batch=3, T=256, Tc=63, r=4, hd=512, ov=1,
+                out=P, stream=NUL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.csa_compress_thd(*[a[n] for n in names])
+
+    for k in ("kv", "score", "cu", "cuc", "out"):
+        assert call(**{k: NUL}) == 1, k
+    assert call(T=-1) == 2
+    assert call(hd=0) == 2
+    assert call(Tc=65) == 2  # 65 groups of 4 need more than 256 rows
+    assert call(r=0) == 3
+    assert call(hd=65537) == 3
+    assert call(Tc=0) == 0  # nothing to pool
+
+
 def test_product_does_not_import_oracle():
     pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
     for dirpath, _, files in os.walk(pkg):
