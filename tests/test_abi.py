@@ -36,6 +36,21 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_library_exports_nothing_undeclared(L):
+    """Every csa_* symbol the shared library exports is an entry point of the
+    header (no internal launcher leaks into the ABI)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    res = subprocess.run([nm, "-D", "--defined-only", csa.library_path], capture_output=True,
+                         text=True, check=True)
+    exported = sorted({ln.split()[-1] for ln in res.stdout.splitlines()
+                       if ln.split() and ln.split()[-1].startswith("csa_")})
+    assert exported == declared_symbols()
+
+
 def test_status_strings(L):
     for code, name in [(0, "CSA_OK"), (1, "CSA_ERR_NULL"), (3, "CSA_ERR_UNSUPPORTED"),
                        (7, "CSA_ERR_TIMEOUT")]:
