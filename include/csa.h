@@ -2,8 +2,8 @@
  * csa.h -- C ABI of the GB300 (sm_103a) forward path of DeepSeek-V4
  * Compressed Sparse Attention (CSA) and its compressor-only mode (HCA) over
  * THD-packed variable-length sequences (and fixed-shape BSND batches), on one
- * GPU, of the backward of its sparse MLA attention and of the indexer's
- * KL-loss gradient.
+ * GPU; of the backward of its sparse MLA attention, the indexer's KL-loss
+ * gradient and the THD compressor core that produces the compressed rows.
  *
  * Sources (web pages, cited by title and section):
  *   [miles#2038]  "PR #2038 完整报告" (radixark/miles): "Enable THD
