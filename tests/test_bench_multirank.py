@@ -60,3 +60,25 @@ def test_layer_accounting_counts_keys():
     assert acc["keys"] == keys
     assert acc["kv_bytes"] == keys * 1024
     assert acc["mla_flops"] == 4 * 512 * 4 * keys
+
+
+def test_layer_accounting_counts_listed_rows():
+    """cmp_keys (the KL gradient's listed rows) = per token the oracle's
+    visible-block count, capped at top-k."""
+    import numpy as np
+
+    import oracle
+    from csa_inputs import packs
+    lengths = (1, 3, 37, 120, 9)
+    layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=8, index_heads=4, index_dim=64)
+    spec = packs.PackSpec("custom", lengths, heads=4, dim=512, win_left=15, layers=(layer,),
+                          seed=1)
+    acc = bench.layer_accounting(spec, layer)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    cuc = oracle.compress_cu_seqlens(cu, 4)
+    T, tc = int(cu[-1]), int(cuc[-1])
+    rng = np.random.default_rng(0)
+    _, _, _, _, nvis = oracle.indexer_topk(rng.standard_normal((T, 4, 64)),
+                                           rng.standard_normal((tc, 64)),
+                                           rng.standard_normal((T, 4)), T, cu, cuc, 4, 8)
+    assert acc["cmp_keys"] == int(np.minimum(nvis, 8).sum())
