@@ -51,6 +51,8 @@ struct MlaArgs {
     int32_t *err;
     int32_t T, Tc, H, D, batch, topk, cmp_ratio, window;
     float softmax_scale;
+    uint32_t epoch = 0;      // set by the launcher: token-claim epoch and slot
+    int32_t claim_slot = 0;
 };
 
 cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);

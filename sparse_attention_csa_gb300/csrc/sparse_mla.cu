@@ -23,9 +23,11 @@
 //     (SW128, K-major) serves S^T as the A operand and, read MN-major, O^T as
 //     the A operand. Accumulators live in tensor memory: S^T in 64 columns,
 //     O^T in 4 x 64 columns.
-//   * Work split. Each CTA takes one contiguous range of tokens, balanced by a
-//     closed-form model of the tiles per token, so that consecutive tokens of
-//     a sequence follow each other in one CTA.
+//   * Work split. CTAs claim runs of consecutive tokens from a per-launch
+//     counter (guided self-scheduling: each run is a quarter of an even share
+//     of the tokens left, 2 to 256), so consecutive tokens of a sequence
+//     mostly follow each other in one CTA, and every CTA finishes at about the
+//     same time whatever the per-token cost or the speed of its SM.
 //   * Key tiles (kinds below) have slot layouts fixed by the token alone, and
 //     a token at an even position runs its tiles in the natural order (window
 //     first), one at an odd position in reverse. The last tile of a token is
@@ -60,6 +62,9 @@
 #include "internal.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
+
+#include <atomic>
+#include <cstdint>
 
 namespace csa {
 
@@ -112,6 +117,7 @@ struct TokenInfo {
     int32_t cmp_first, flags, b0, n_top;     // first compressed row (runs); ring base
     int32_t n_wt, n_ct, n_tiles, single;     // window / compressed / all tiles; single-tile kind or -1
     int32_t reuse, n_delta;                  // first tile taken over from the previous token
+    int32_t end;                             // no token: the CTA's stream ends here
     int32_t d_row[2], d_slot[2], d_cmp[2];   // rows loaded into it (d_cmp: from cmp_kv)
 };
 
@@ -160,145 +166,41 @@ __device__ __forceinline__ bool slot_valid(const TokenInfo &ti, const TileDesc &
     return r >= ti.win_start;
 }
 
-// ---------------------------------------------------------------- work split
-// Each CTA runs one contiguous range of tokens, so consecutive tokens of a
-// sequence meet in the same CTA. The ranges split a work model evenly: a token
-// costs kTokenCost plus kTileCost per key tile (the time goes mostly per tile).
-// With nw(p) = min(W, p+1) window keys and nc(p) = min(Kcap, floor((p+1)/r))
-// compressed keys at position p, a token has one tile when nw + nc <= 128,
-// else ceil(nw/128) + ceil(nc/128) (one ring tile when W <= 128). The prefix
-// sums over a sequence are closed forms over the few positions where a
-// ceiling steps. Compressed tiles gathered from a top-k list (positions that
-// see more blocks than top-k keeps) cost a little more than boxed runs. The
-// three weights are a least-squares fit of measured per-CTA times (GB300,
-// one 152-CTA launch per layer, five layers of 4k-32k-token packs): about 1.7 us a
-// token, 3.8 us a tile and 0.5 us more for a gathered tile.
-constexpr int64_t kTokenCost = 11;
-constexpr int64_t kTileCost = 24;
-constexpr int64_t kGatherCost = 3;  // extra for a compressed tile gathered from a top-k list
+// ------------------------------------------------------------ token claims
+// CTAs take runs of consecutive tokens from the claim word of the launch's
+// slot (dynamic, guided self-scheduling: a run is a share of what is left, so
+// runs shrink towards the end of the launch and every CTA finishes at about
+// the same time whatever the per-token cost). The high half of a word holds
+// the epoch of the launch using it and the low half the tokens claimed so far.
+// The last CTA to finish resets the word, so a launch replayed with the same
+// epoch (a captured graph) starts afresh; a word left behind by a launch that
+// gave up is recognised by its older epoch. Launches in flight at the same
+// time take different slots (one per launch, cycling through kClaimSlots); a
+// claim that finds another launch's epoch in the word reports it.
+constexpr int kClaimSlots = 1024;
+__device__ unsigned long long g_claim[kClaimSlots];
+__device__ unsigned int g_claim_done[kClaimSlots];
 
-struct WorkModel {
-    int64_t W, r, kcap;  // kcap < 0: no cap; r == 0: no compressed keys
-    int64_t p1;          // first position with more than one tile
-    __device__ __forceinline__ int64_t nc(int64_t p) const {
-        if (r <= 0) return 0;
-        const int64_t v = (p + 1) / r;
-        return kcap < 0 ? v : min(v, kcap);
-    }
-    __device__ __forceinline__ int64_t keys(int64_t p) const { return min(W, p + 1) + nc(p); }
-    __device__ void init(int64_t W_, int64_t r_, int64_t kcap_) {
-        W = W_;
-        r = r_;
-        kcap = kcap_;
-        // keys(p) grows with p and exceeds 128 by p = 128 at the latest
-        int64_t lo = 0, hi = kTileKeys;
-        while (lo < hi) {
-            const int64_t mid = (lo + hi) >> 1;
-            if (keys(mid) > kTileKeys) hi = mid;
-            else lo = mid + 1;
+// First token of a run of n claimed by this launch (>= T once all are taken;
+// INT64_MAX when the word belongs to another launch).
+__device__ int64_t claim_run(unsigned long long *w, uint32_t epoch, uint32_t n) {
+    const unsigned long long mine = ((unsigned long long)epoch << 32) | n;
+    unsigned long long v = atomicAdd(w, (unsigned long long)n);
+    if ((uint32_t)(v >> 32) == epoch) return (int64_t)(uint32_t)v;
+    // The word is not this launch's yet: install this launch's epoch with this
+    // run as its first claim, unless another CTA of the launch already did.
+    unsigned long long cur = v + n;
+    for (int tries = 0; tries < 4096; ++tries) {
+        const unsigned long long prev = atomicCAS(w, cur, mine);
+        if (prev == cur) return 0;
+        if ((uint32_t)(prev >> 32) == epoch) {
+            v = atomicAdd(w, (unsigned long long)n);
+            if ((uint32_t)(v >> 32) != epoch) break;
+            return (int64_t)(uint32_t)v;
         }
-        p1 = lo;
+        cur = prev;
     }
-    // #{p in [a, b) : nc(p) > 128 k}, summed over k >= 0
-    __device__ __forceinline__ int64_t cmp_tiles(int64_t a, int64_t b) const {
-        int64_t s = 0;
-        if (r <= 0) return 0;
-        for (int64_t k = 0;; ++k) {
-            if (kcap >= 0 && kcap <= kTileKeys * k) break;
-            const int64_t thr = r * (kTileKeys * k + 1) - 1;  // nc(p) > 128 k  <=>  p >= thr
-            if (thr >= b) break;
-            s += b - max(a, thr);
-        }
-        return s;
-    }
-    // #{p in [a, b) : nw(p) > 128 k}, summed over k >= 0
-    __device__ __forceinline__ int64_t win_tiles(int64_t a, int64_t b) const {
-        int64_t s = 0;
-        for (int64_t k = 0; W > kTileKeys * k && kTileKeys * k < b; ++k)
-            s += b - max(a, kTileKeys * k);
-        return s;
-    }
-    // cost of the first P positions of a sequence
-    __device__ int64_t prefix(int64_t P) const {
-        if (P <= 0) return 0;
-        int64_t tiles = min(P, p1), gathered = 0;
-        if (p1 < P) {
-            tiles += (W <= kTileKeys ? P - p1 : win_tiles(p1, P)) + cmp_tiles(p1, P);
-            if (r > 0 && kcap >= 0) {  // positions that see more blocks than top-k keeps
-                const int64_t pg = max(p1, r * (kcap + 1) - 1);
-                if (P > pg) gathered = (P - pg) * ((kcap + kTileKeys - 1) / kTileKeys);
-            }
-        }
-        return kTokenCost * P + kTileCost * tiles + kGatherCost * gathered;
-    }
-};
-
-// [*lo, *hi) for this CTA; run by one whole warp.
-__device__ void cta_token_range(const MlaArgs &a, bool use_cmp, int lane, int32_t *lo,
-                                int32_t *hi) {
-    WorkModel wm;
-    wm.init(a.window, use_cmp ? a.cmp_ratio : 0, a.cmp_idx ? a.topk : -1);
-    const int64_t G = gridDim.x, c = blockIdx.x;
-    // pass 1: total cost and a sanity check of cu_seqlens
-    int64_t total = 0;
-    bool sane = a.batch >= 0 && __ldg(a.cu_q) >= 0 && __ldg(a.cu_q + a.batch) <= a.T;
-    for (int32_t b0 = 0; b0 < a.batch; b0 += 32) {
-        const int32_t b = b0 + lane;
-        int64_t cost = 0;
-        if (b < a.batch) {
-            const int32_t L = __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b);
-            sane &= L >= 0;
-            cost = wm.prefix(max(L, 0));
-        }
-        for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
-        total += cost;
-    }
-    sane = __all_sync(0xffffffffu, sane);
-    if (!sane || total <= 0) {  // fall back to an even split of the token range
-        if (!sane && lane == 0 && c == 0) report_error(a.err, kErrCheck, kKerMla, 3);
-        *lo = (int32_t)((int64_t)a.T * c / G);
-        *hi = (int32_t)((int64_t)a.T * (c + 1) / G);
-        return;
-    }
-    const int64_t S[2] = {total * c / G, total * (c + 1) / G};
-    int32_t res[2] = {a.T, a.T};
-    int64_t carry = 0;
-    for (int32_t b0 = 0; b0 < a.batch; b0 += 32) {
-        const int32_t b = b0 + lane;
-        int64_t cost = 0;
-        int32_t L = 0, start = 0;
-        if (b < a.batch) {
-            start = __ldg(a.cu_q + b);
-            L = __ldg(a.cu_q + b + 1) - start;
-            cost = wm.prefix(L);
-        }
-        int64_t incl = cost;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const int64_t before = carry + incl - cost;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            // first token whose preceding cost reaches S[k]
-            const bool mine = cost > 0 && before <= S[k] && S[k] < before + cost;
-            int32_t t = a.T;
-            if (mine) {
-                int64_t lo_p = 0, hi_p = L;  // smallest P with before + prefix(P) >= S
-                while (lo_p < hi_p) {
-                    const int64_t mid = (lo_p + hi_p) >> 1;
-                    if (before + wm.prefix(mid) >= S[k]) hi_p = mid;
-                    else lo_p = mid + 1;
-                }
-                t = start + (int32_t)lo_p;
-            }
-            const uint32_t m = __ballot_sync(0xffffffffu, mine);
-            if (m) res[k] = __shfl_sync(0xffffffffu, t, __ffs(m) - 1);
-        }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    *lo = c == 0 ? 0 : res[0];
-    *hi = c == G - 1 ? a.T : res[1];
+    return INT64_MAX;
 }
 
 struct Misc {
@@ -308,7 +210,6 @@ struct Misc {
     uint64_t info_full[2], info_empty[2];
     uint32_t tmem_base;
     int32_t abort;
-    int32_t range_lo, range_hi;  // this CTA's tokens
     TokenInfo info[2];
     __align__(16) float red[2][4][64];   // [tile parity][lane quarter][head]
     __align__(16) float sink2[64];       // sink * log2(e), -inf when absent
@@ -464,18 +365,11 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             tc::tma_prefetch_desc(&ori_map);
             tc::tma_prefetch_desc(&cmp_map);
         }
-        int32_t lo, hi;
-        cta_token_range(a, use_cmp, lane, &lo, &hi);
-        if (lane == 0) {
-            ms->range_lo = lo;
-            ms->range_hi = hi;
-        }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const int32_t t_lo = ms->range_lo, t_hi = ms->range_hi;
 
     if (warp == 0) {
         // ================================================== scheduler warp
@@ -492,12 +386,32 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const int32_t e = 32 * r + lane;
-                jn[r] = (a.cmp_idx && tt < t_hi && e < a.topk) ? __ldg(a.cmp_idx + (int64_t)tt * a.topk + e)
+                jn[r] = (a.cmp_idx && tt < a.T && e < a.topk) ? __ldg(a.cmp_idx + (int64_t)tt * a.topk + e)
                                                                : -1;
             }
         };
-        load_first_round(t_lo);
-        for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
+        // Runs of tokens claimed from the launch's claim word: a quarter of an
+        // even share of what is left, 2 to 256 tokens.
+        unsigned long long *claim_word = &g_claim[a.claim_slot];
+        int32_t run_end = 0;
+        auto claim = [&]() -> int32_t {
+            int64_t start = 0;
+            uint32_t n = 0;
+            if (lane == 0) {
+                const int64_t left = max((int64_t)a.T - (int64_t)run_end, (int64_t)0);
+                n = (uint32_t)min(max(left / (4 * (int64_t)gridDim.x), (int64_t)2), (int64_t)256);
+                start = claim_run(claim_word, a.epoch, n);
+                if (start == INT64_MAX) report_error(a.err, kErrCheck, kKerMla, 4);
+            }
+            start = __shfl_sync(0xffffffffu, start, 0);
+            n = __shfl_sync(0xffffffffu, n, 0);
+            if (start >= a.T) return a.T;
+            run_end = (int32_t)min(start + (int64_t)n, (int64_t)a.T);
+            return (int32_t)start;
+        };
+        int32_t t = claim();
+        load_first_round(t);
+        for (; t < a.T; ++it) {
             const uint32_t slot = it & 1;
             // the slot's key list is rewritten only once every consumer is done
             bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
@@ -639,30 +553,41 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 bs_t = t;
                 bs_row0 = l.row0;
             }
+            // the token after this one: the next of the run, or a new run's first
+            const int32_t next = t + 1 < run_end ? t + 1 : claim();
             __syncwarp();  // list writes before the release below
             if (lane == 0) {
                 ms->info[slot] = ti;
                 tc::mbar_arrive(&ms->info_full[slot]);
                 // Q of the next token streams from HBM into L2 while this token
                 // runs; its TMA load then hits L2.
-                if (t + 1 < t_hi)
-                    tc::prefetch_l2_bulk(a.q + (int64_t)(t + 1) * a.H * 512, (uint32_t)a.H * 1024u);
+                if (next < a.T)
+                    tc::prefetch_l2_bulk(a.q + (int64_t)next * a.H * 512, (uint32_t)a.H * 1024u);
             }
-            if (!ti.valid) {
-                load_first_round(t + 1);
-                continue;
+            if (ti.valid) {
+                // Q rows of token t (H rows of 512; rows >= H stay zero), once
+                // the previous token's last S^T has read its Q
+                ok = cx.wait(&ms->q_empty, (q_n & 1) ^ 1, 11);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                if (lane == 0) {
+                    tc::mbar_expect_tx(&ms->q_full, 8u * a.H * 128u);
+                    for (int c = 0; c < 8; ++c)
+                        tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full, 64 * c, 0, t);
+                }
+                ++q_n;
             }
-            // Q rows of token t (H rows of 512; rows >= H stay zero), once the
-            // previous token's last S^T has read its Q
-            ok = cx.wait(&ms->q_empty, (q_n & 1) ^ 1, 11);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            if (lane == 0) {
-                tc::mbar_expect_tx(&ms->q_full, 8u * a.H * 128u);
-                for (int c = 0; c < 8; ++c)
-                    tc::tma_load_3d(smem + kOffQ + c * 8192, &q_map, &ms->q_full, 64 * c, 0, t);
+            load_first_round(next);
+            t = next;
+        }
+        if (t >= a.T) {  // the end marker, once the slot is free
+            const uint32_t slot = it & 1;
+            const bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 12);
+            if (__all_sync(0xffffffffu, ok) && lane == 0) {
+                TokenInfo ti = {};
+                ti.end = 1;
+                ms->info[slot] = ti;
+                tc::mbar_arrive(&ms->info_full[slot]);
             }
-            ++q_n;
-            load_first_round(t + 1);
         }
         if (lane == 0 && q_n > 0)  // drain: every Q copy issued has landed
             if (!tc::mbar_wait(&ms->q_full, (q_n - 1) & 1)) cx.fail(13);
@@ -682,10 +607,11 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         uint32_t it = 0, kf_n = 0;
         const uint32_t kv_base = tc::smem_u32(smem + kOffKV);
         bool stop = false;
-        for (int32_t t = t_lo; t < t_hi && !stop; ++t, ++it) {
+        for (; !stop; ++it) {
             const uint32_t slot = it & 1;
             if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40)) break;
             const TokenInfo &ti = ms->info[slot];  // released after this token's loads
+            if (ti.end) break;
             const int32_t *list = reinterpret_cast<const int32_t *>(smem + kOffList) + slot * kMaxList;
             const int32_t n_tiles = ti.valid ? ti.n_tiles : 0;
             for (int32_t j = 0; j < n_tiles && !stop; ++j) {
@@ -803,9 +729,10 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             const uint64_t do_b = tc::smem_desc(tc::smem_u32(smem + kOffP), 16384, 1024);
             uint32_t it = 0, q_n = 0, kf_n = 0, p_n = 0;
             bool issued = false;
-            for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
+            for (;; ++it) {
                 const uint32_t slot = it & 1;
                 if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
+                if (ms->info[slot].end) break;
                 const int32_t n_tiles = ms->info[slot].valid ? ms->info[slot].n_tiles : 0;
                 // a first tile taken over whole needs no load
                 const bool first_loaded = !(ms->info[slot].reuse && ms->info[slot].n_delta == 0);
@@ -846,14 +773,14 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     // next tile loads into it: the next token's info decides
                     // for this token's last tile.
                     bool release = true;
-                    if (j == n_tiles - 1 && t + 1 < t_hi) {
+                    if (j == n_tiles - 1) {
                         const uint32_t ns = (it + 1) & 1;
                         if (!cx.wait(&ms->info_full[ns], ((it + 1) >> 1) & 1, 25)) {
                             stop = true;
                             break;
                         }
                         const TokenInfo &nx = ms->info[ns];
-                        release = !(nx.valid && nx.reuse && nx.n_delta == 0);
+                        release = !(!nx.end && nx.valid && nx.reuse && nx.n_delta == 0);
                     }
                     tc::tc_fence_after();
                     for (int s = 0; s < 4; ++s) {
@@ -890,11 +817,13 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         unsigned char *pbuf = smem + kOffP;
         const float c = a.softmax_scale * kLog2e;
         uint32_t it = 0, s_n = 0, o_n = 0, tile_ctr = 0;
-        for (int32_t t = t_lo; t < t_hi; ++t, ++it) {
+        for (;; ++it) {
             const uint32_t slot = it & 1;
             bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
             if (!bar_red_and(bar_id, ok)) break;
-            const TokenInfo &ti = ms->info[slot];  // released at the end of the token
+            const TokenInfo ti = ms->info[slot];  // a register copy; the slot is released at the end
+            if (ti.end) break;
+            const int32_t t = ti.t;
             if (!ti.valid) {
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
@@ -911,8 +840,12 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             for (int i = 0; i < 32; ++i) m_cur[i] = __shfl_sync(0xffffffffu, m_lane, i);
             bool stop = false;
             for (int32_t j = 0; j < ti.n_tiles; ++j, ++tile_ctr) {
+                // whether this thread's slot holds a key: known before the scores
+                const bool key_ok = slot_valid(ti, tile_at(ti, tile_nat(ti, j)), row);
                 ok = cx.wait(&ms->s_full, s_n & 1, 31);
-                if (!bar_red_and(bar_id, ok)) {
+                // A token's first tile agrees on the wait here; later tiles fold
+                // it into the max vote below (one barrier per tile).
+                if (j == 0 && !bar_red_and(bar_id, ok)) {
                     stop = true;
                     break;
                 }
@@ -921,7 +854,6 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 float v[32];
                 tc::tmem_ld32(lane_addr + kColS + h0, v);
                 tc::tmem_wait_ld();
-                const bool key_ok = slot_valid(ti, tile_at(ti, tile_nat(ti, j)), row);
                 if (j == 0) {
                     // A token's first tile sets the max exactly: the max of the
                     // sink and the tile's scores, so the largest probability is
@@ -949,10 +881,15 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     // of a tile exceeds it by more than kLazyMax: the warpgroup
                     // first checks whether any does, and only then reduces the
                     // tile maxima.
-                    bool exceeds = false;
+                    bool exceeds = !ok;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) exceeds |= v[i] > kLazyMax;
                     if (bar_red_or(bar_id, exceeds)) {
+                        // rare: some head's max moves, or some wait gave up
+                        if (!bar_red_and(bar_id, ok)) {
+                            stop = true;
+                            break;
+                        }
                         // the scaled scores again (S^T is still in tensor memory)
                         tc::tmem_ld32(lane_addr + kColS + h0, v);
                         tc::tmem_wait_ld();
@@ -1064,6 +1001,13 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     __syncthreads();
     tc::tc_fence_after();
     if (warp == 3) tc::tmem_dealloc(tmem, kTmemCols);
+    if (tid == 0) {  // the last CTA out resets the launch's claim word
+        __threadfence();
+        if (atomicAdd(&g_claim_done[a.claim_slot], 1u) == gridDim.x - 1) {
+            atomicExch(&g_claim[a.claim_slot], 0ull);
+            atomicExch(&g_claim_done[a.claim_slot], 0u);
+        }
+    }
 }
 
 }  // namespace
@@ -1088,8 +1032,13 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    // Each launch takes a fresh epoch and the claim slot it selects.
+    static std::atomic<uint32_t> epochs{0};
+    MlaArgs la = a;
+    la.epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;
+    la.claim_slot = (int32_t)(la.epoch % kClaimSlots);
     const int ctas = a.T < sms ? a.T : sms;
-    sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, a);
+    sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, la);
     return cudaGetLastError();
 }
 

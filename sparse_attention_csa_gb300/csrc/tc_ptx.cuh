@@ -61,15 +61,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` of wall time. Returns false on timeout (the caller records the
 // error and drains); never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
     while (true) {
+#pragma unroll 1
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, limit_ns);
 }
 
 // --------------------------------------------------------------------- fences
