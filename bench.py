@@ -342,16 +342,16 @@ def cpu_baseline(layers, seconds):
 
 
 # --------------------------------------------------------------------------- arms
-def traffic_record(kernel_name):
+def traffic_record(kernel_name, config, layer):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current kernel source, for the same workload and layer; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel_name)
     except (OSError, ValueError):
         return None
-    if not rec:
+    if not rec or rec.get("config") != config or rec.get("layer") != layer:
         return None
     src = os.path.join(ROOT, "sparse_attention_csa_gb300", "csrc", rec["source"])
     try:
@@ -434,7 +434,7 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"]}
         extra = {}
-    roof["traffic"] = traffic_record(dom.split("/")[0])
+    roof["traffic"] = traffic_record(dom.split("/")[0], spec.name, dom.split("/")[1])
     roof.update({"kernel": dom, "kernel_ms": avg[dom], "peak_source": peak_kind, **extra})
     # path-level roofline as the method defines it: max(gathered bytes/BW, flops/peak)
     bytes_all = sum(L.acc["kv_bytes"] for L in layers)

@@ -28,8 +28,10 @@
 //     order with warp scans.
 //   * A token that sees at most topk blocks selects all of them whatever
 //     their scores, so unless the caller asks for the values it is not scored
-//     at all (its row is written by the selection's n <= k path); a group
-//     with no token left to score loads and multiplies nothing.
+//     at all: a first pass marks the CTA's groups that hold a token to score,
+//     only those go through the pipeline, and the four epilogue warps write
+//     every other row (16-byte stores) while the pipeline's loads and first
+//     MMAs run.
 //   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
 //     and selection. Every mbarrier wait is bounded.
 #include "common.cuh"
@@ -47,6 +49,7 @@ constexpr int kTileRows = 128;      // compressed rows per MMA tile
 constexpr int kScoreCap = 5120;     // rows per token kept in shared memory
 constexpr int kMaxCtas = 1024;      // persistent grid bound (sizes the scratch)
 constexpr int kCuCap = 500;         // sequences whose offsets are staged in shared memory
+constexpr int kGrpBits = 4096;      // groups per CTA tracked by the scored-group bitmap
 
 // shared memory map (1024-aligned base)
 constexpr uint32_t kOffB = 0;                 // q group: 2 chunks x [256 rows x 128 B]
@@ -77,6 +80,7 @@ struct Misc {
     float w[kG * 64];
     int32_t hist[4][256];
     int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
+    uint32_t gscored[kGrpBits / 32];             // this CTA's groups with a token to score
 };
 
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
@@ -249,6 +253,37 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         tc::tma_prefetch_desc(&q_map);
         tc::tma_prefetch_desc(&k_map);
     }
+    // This CTA's groups are blockIdx.x + k gridDim.x. Unless values are
+    // requested, a first pass marks those holding a token to score; only they
+    // go through the pipeline below, and the epilogue warps write the other
+    // rows (all visible blocks, then -1) before they start on it.
+    const int64_t my_groups =
+        blockIdx.x < (uint32_t)n_groups ? (n_groups - 1 - (int64_t)blockIdx.x) / gridDim.x + 1 : 0;
+    const bool bulk = a.topk_val == nullptr && my_groups <= kGrpBits;
+    const int32_t *cq = cu_smem ? ms->cu_q : a.cu_q;
+    const int32_t *cc = cu_smem ? ms->cu_c : a.cu_c;
+    // Visible rows of token t (0 when none; -1 when t is outside the pack or
+    // the offsets are inconsistent, reported) and their first row.
+    auto visible = [&](int32_t t, int32_t *cb) -> int32_t {
+        const int32_t seg = cu_smem ? find_segment_smem(cq, a.batch, t) : find_segment(cq, a.batch, t);
+        *cb = 0;
+        if (seg < 0) return -1;
+        if (a.Tc <= 0) return 0;
+        const int32_t pos = t - cq[seg];
+        *cb = cc[seg];
+        const int32_t n = min((pos + 1) / a.cmp_ratio, cc[seg + 1] - *cb);
+        return (*cb < 0 || n < 0 || (int64_t)*cb + n > a.Tc) ? -2 : n;
+    };
+    for (int i = tid; i < kGrpBits / 32; i += kThreads) ms->gscored[i] = 0;
+    __syncthreads();
+    if (bulk) {
+        for (int64_t li = tid; li < my_groups * kG; li += kThreads) {
+            const int64_t k = li / kG;
+            const int32_t t = (int32_t)(((int64_t)blockIdx.x + k * gridDim.x) * kG + li % kG);
+            int32_t cb;
+            if (t < a.T && visible(t, &cb) > a.topk) atomicOr(&ms->gscored[k >> 5], 1u << (k & 31));
+        }
+    }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -258,7 +293,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // ===================================================== producer warp
         uint32_t it = 0, b_n = 0, a_n = 0;
         bool quit = false;
-        for (int32_t grp = blockIdx.x; grp < n_groups && !quit; grp += gridDim.x) {
+        int64_t kg = 0;
+        for (int32_t grp = blockIdx.x; grp < n_groups && !quit; grp += gridDim.x, ++kg) {
+            // rows already written by the bulk pass and nothing to score
+            if (bulk && !((ms->gscored[kg >> 5] >> (kg & 31)) & 1u)) continue;
             GroupInfo gi;
             gi.t0 = grp * kG;
             gi.n_pass = 0;
@@ -458,6 +496,45 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         const int sel_warp = warp - 2;  // token of the group this warp selects for
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
+        // Rows of the groups with nothing to score, written first (while the
+        // producer and the MMA warp start on the scored groups): 32 tokens found
+        // at a time per warp, one row per warp store round (16-byte stores
+        // when aligned).
+        if (bulk) {
+            const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
+            for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += 128) {
+                const int64_t li = base + lane;
+                const int64_t k = li / kG;
+                int32_t t = -1, n = 0, cb = 0;
+                bool write = false;
+                if (li < my_groups * kG && !((ms->gscored[k >> 5] >> (k & 31)) & 1u)) {
+                    t = (int32_t)(((int64_t)blockIdx.x + k * gridDim.x) * kG + li % kG);
+                    if (t < a.T) {
+                        write = true;
+                        n = visible(t, &cb);
+                        if (n < 0) {
+                            report_error(a.err, kErrCheck, kKerIndexer, n == -1 ? 1 : 2);
+                            n = 0;
+                        }
+                    }
+                }
+                for (uint32_t m = __ballot_sync(0xffffffffu, write); m; m &= m - 1) {
+                    const int src = __ffs(m) - 1;
+                    const int32_t tw = __shfl_sync(0xffffffffu, t, src);
+                    const int32_t nw = __shfl_sync(0xffffffffu, n, src);
+                    const int32_t cw = __shfl_sync(0xffffffffu, cb, src);
+                    int32_t *idx_row = a.topk_idx + (int64_t)tw * a.topk;
+                    if (vec) {
+                        for (int32_t i = 4 * lane; i < a.topk; i += 128)
+                            *reinterpret_cast<int4 *>(idx_row + i) =
+                                make_int4(i < nw ? cw + i : -1, i + 1 < nw ? cw + i + 1 : -1,
+                                          i + 2 < nw ? cw + i + 2 : -1, i + 3 < nw ? cw + i + 3 : -1);
+                    } else {
+                        for (int32_t i = lane; i < a.topk; i += 32) idx_row[i] = i < nw ? cw + i : -1;
+                    }
+                }
+            }
+        }
         uint32_t it = 0, t_n = 0;
         for (;; ++it) {
             const uint32_t slot = it & 1;
