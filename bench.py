@@ -12,6 +12,10 @@ One step = the whole path for both layers: compressed cu_seqlens, window
 rows, indexer + top-k (CSA layer), sparse MLA with sinks. Inputs are resident
 in HBM when the timed region starts; L2 is flushed (a 256 MB write) between
 steps, outside the per-step CUDA events. ``value`` is tokens / device time.
+The timed steps record events only before each step and after each layer (the
+kernels of a layer are launched back to back, each allowed to start while the
+one before it finishes); per-kernel times come from separate steps after the
+timed region, with an event after every launch.
 
 Extra objects on the JSON line:
 * roofline  -- the dominant kernel's algorithmic bytes (gathered KV rows,
@@ -187,14 +191,15 @@ class Layer:
             self.ws = torch.empty(need, dtype=torch.uint8, device=device) if need else None
         self.acc = layer_accounting(spec, layer)
 
-    def launches(self, stream, events=None, names=None):
-        """Run the layer; optionally record an event after each launch."""
+    def launches(self, stream, events=None, names=None, per_kernel=True):
+        """Run the layer; optionally record an event after each launch
+        (per_kernel) or only after the layer's last one."""
         import sparse_attention_csa_gb300 as csa
         d, L, spec = self.dev, self.layer, self.spec
         n = 0
 
-        def mark(name):
-            if events is not None:
+        def mark(name, last=False):
+            if events is not None and (per_kernel or last):
                 e = torch.cuda.Event(enable_timing=True)
                 e.record(stream)
                 events.append(e)
@@ -218,7 +223,7 @@ class Layer:
                                d["sinks"], spec.scale, L.cmp_ratio, spec.win_left, 0, True,
                                out=self.out, lse=self.lse, stream=stream)
         n += 1
-        mark(f"sparse_mla_fwd/r{L.cmp_ratio}")
+        mark(f"sparse_mla_fwd/r{L.cmp_ratio}" if per_kernel else f"layer/r{L.cmp_ratio}", last=True)
         return n
 
 
@@ -372,8 +377,8 @@ def run_ours(args, world, rank, local):
 
     import sparse_attention_csa_gb300 as csa
 
-    def step(events=None, names=None):
-        return sum(L.launches(stream, events, names) for L in layers)
+    def step(events=None, names=None, per_kernel=True):
+        return sum(L.launches(stream, events, names, per_kernel) for L in layers)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -390,26 +395,40 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     wall0 = time.perf_counter()
+    # Timed steps: events before the step and after each layer only, so that the
+    # launches of a layer follow each other with nothing in between (each
+    # kernel may then start while the one before it finishes).
     recs = []
     for _ in range(args.steps):
         flush.zero_()
         ev = [torch.cuda.Event(enable_timing=True)]
         ev[0].record(stream)
         nm = []
-        launches += step(ev, nm)
+        launches += step(ev, nm, per_kernel=False)
         recs.append((ev, nm))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
     clk = clocks.stop()
+    layer_ms = {}
     for ev, nm in recs:
         step_ms.append(ev[0].elapsed_time(ev[-1]))
         for i, n in enumerate(nm):
-            kern_ms.setdefault(n, []).append(ev[i].elapsed_time(ev[i + 1]))
-        names = nm
+            layer_ms.setdefault(n, []).append(ev[i].elapsed_time(ev[i + 1]))
     st, word = csa.csa_device_error()
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {word:#x}")
+    # Per-kernel breakdown (dominant kernel, kernels_ms): separate steps with an
+    # event after every launch, after the timed region.
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True)]
+        ev[0].record(stream)
+        nm = []
+        step(ev, nm)
+        torch.cuda.synchronize()
+        for i, n in enumerate(nm):
+            kern_ms.setdefault(n, []).append(ev[i].elapsed_time(ev[i + 1]))
 
     agg = aggregate(step_ms, T, world, device)
     value, ms_per_step = agg["value"], agg["ms_per_step"]
@@ -445,7 +464,7 @@ def run_ours(args, world, rank, local):
     per_layer = {}
     for L in layers:
         r = L.layer.cmp_ratio
-        lt = sum(avg[n] for n in avg if n.endswith(f"/r{r}"))
+        lt = statistics.mean(layer_ms[f"layer/r{r}"])
         tl = max(L.acc["kv_bytes"] / (peaks["hbm_gbs"] * 1e9),
                  (L.acc["mla_flops"] + L.acc["idx_flops"]) / (peaks["bf16_tflops"] * 1e12))
         per_layer[f"r{r}"] = {"ms": lt, "roofline_ms": tl * 1e3, "frac": tl * 1e3 / lt}
@@ -463,6 +482,8 @@ def run_ours(args, world, rank, local):
                                + f", H={spec.heads}, D={spec.dim}, window {spec.win_left + 1}",
                    "tokens_per_step": T, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between steps (256 MB write, outside the step events)",
+                   "timing": "events at step and layer boundaries; per-kernel times from "
+                             "separate steps with an event after every launch",
                    "indexer_values": "not requested: tokens whose visible blocks fit in top-k "
                                      "keep them all unscored",
                    "wall_ms_incl_flush": wall * 1e3 / args.steps},

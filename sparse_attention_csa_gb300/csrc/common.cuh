@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "csa.h"
 
 namespace csa {
@@ -116,6 +118,41 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t *scra
     *total = scratch[NT / 32];
     __syncthreads();
     return before;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. The forward kernels are launched so that they
+// may start while the kernel before them on the stream finishes: each one does
+// its purely local set-up (barriers, tensor memory, shared memory), then waits
+// here for the grids it depends on to complete with their memory visible,
+// before its first global read or write. For a launch that did not start early
+// the wait returns at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel on the stream (if launched the same way) be scheduled;
+// its CTAs still wait in grid_dependency_wait until this grid has completed.
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization (see grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_early(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace csa

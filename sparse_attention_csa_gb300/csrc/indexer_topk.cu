@@ -238,13 +238,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         ms->abort = 0;
         tc::fence_mbar_init();
     }
-    // The producer looks up every token's sequence: keep the offsets on chip.
-    const bool cu_smem = a.batch <= kCuCap;
-    if (cu_smem)
-        for (int i = tid; i <= a.batch; i += kThreads) {
-            ms->cu_q[i] = __ldg(a.cu_q + i);
-            ms->cu_c[i] = a.Tc > 0 ? __ldg(a.cu_c + i) : 0;
-        }
     if (warp == 1) {
         tc::tmem_alloc(&ms->tmem_base, 512);
         tc::tmem_relinquish();
@@ -253,6 +246,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         tc::tma_prefetch_desc(&q_map);
         tc::tma_prefetch_desc(&k_map);
     }
+    // everything above is local: wait for the kernels before this one
+    grid_dependency_wait();
+    launch_dependents();
+    // The producer looks up every token's sequence: keep the offsets on chip.
+    const bool cu_smem = a.batch <= kCuCap;
+    if (cu_smem)
+        for (int i = tid; i <= a.batch; i += kThreads) {
+            ms->cu_q[i] = __ldg(a.cu_q + i);
+            ms->cu_c[i] = a.Tc > 0 ? __ldg(a.cu_c + i) : 0;
+        }
     // This CTA's groups are blockIdx.x + k gridDim.x. Unless values are
     // requested, a first pass marks those holding a token to score; only they
     // go through the pipeline below, and the epilogue warps write the other
@@ -628,8 +631,8 @@ cudaError_t launch_t(const IndexerArgs &a, const CUtensorMap &qm, const CUtensor
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    indexer_tc_kernel<HPAD, DI><<<ctas, kThreads, kSmemBytes, stream>>>(qm, km, a);
-    return cudaGetLastError();
+    return launch_early(indexer_tc_kernel<HPAD, DI>, dim3(ctas), dim3(kThreads), kSmemBytes, stream,
+                        qm, km, a);
 }
 
 template <int DI>

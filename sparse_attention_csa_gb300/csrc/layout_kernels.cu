@@ -20,6 +20,8 @@ compress_cu_seqlens_kernel(const int32_t *__restrict__ cu, int32_t batch, int32_
                            int32_t *__restrict__ cu_cmp, int32_t *err) {
     __shared__ int32_t scratch[NT / 32 + 1];
     int32_t carry = 0;
+    grid_dependency_wait();
+    launch_dependents();
     if (threadIdx.x == 0) cu_cmp[0] = 0;
     for (int32_t base = 0; base < batch; base += NT) {
         const int32_t b = base + threadIdx.x;
@@ -51,6 +53,8 @@ window_idx_kernel(const int32_t *__restrict__ cu, int32_t batch, int32_t T, int3
     const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t per = (T + warps - 1) / warps;
     const int64_t t0 = w * per, t1 = min((int64_t)T, t0 + per);
+    grid_dependency_wait();
+    launch_dependents();
     if (t0 >= t1) return;
     int32_t b = -1, seg0 = 0, seg1 = 0;
     for (int64_t t = t0; t < t1; ++t) {
@@ -91,10 +95,10 @@ window_idx_kernel(const int32_t *__restrict__ cu, int32_t batch, int32_t T, int3
 cudaError_t launch_compress_cu_seqlens(const int32_t *cu, int32_t batch, int32_t cmp_ratio,
                                        int32_t *cu_cmp, int32_t *err, cudaStream_t stream) {
     if (batch <= 128)
-        compress_cu_seqlens_kernel<128><<<1, 128, 0, stream>>>(cu, batch, cmp_ratio, cu_cmp, err);
-    else
-        compress_cu_seqlens_kernel<1024><<<1, 1024, 0, stream>>>(cu, batch, cmp_ratio, cu_cmp, err);
-    return cudaGetLastError();
+        return launch_early(compress_cu_seqlens_kernel<128>, dim3(1), dim3(128), 0, stream, cu,
+                            batch, cmp_ratio, cu_cmp, err);
+    return launch_early(compress_cu_seqlens_kernel<1024>, dim3(1), dim3(1024), 0, stream, cu, batch,
+                        cmp_ratio, cu_cmp, err);
 }
 
 cudaError_t launch_window_idx(const int32_t *cu, int32_t batch, int32_t total_tokens,
@@ -110,9 +114,8 @@ cudaError_t launch_window_idx(const int32_t *cu, int32_t batch, int32_t total_to
     int64_t blocks = ((int64_t)total_tokens + 4 * warps_per_block - 1) / (4 * warps_per_block);
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     const bool vec4 = (window & 3) == 0 && ((uintptr_t)idx & 15u) == 0;
-    window_idx_kernel<<<(unsigned)blocks, 32 * warps_per_block, 0, stream>>>(
-        cu, batch, total_tokens, window, vec4, idx, err);
-    return cudaGetLastError();
+    return launch_early(window_idx_kernel, dim3((unsigned)blocks), dim3(32 * warps_per_block), 0,
+                        stream, cu, batch, total_tokens, window, vec4, idx, err);
 }
 
 }  // namespace csa

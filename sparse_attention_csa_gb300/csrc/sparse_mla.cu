@@ -348,8 +348,6 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         ms->abort = 0;
         tc::fence_mbar_init();
     }
-    if (tid < 64)
-        ms->sink2[tid] = (a.sinks && tid < a.H) ? __ldg(a.sinks + tid) * kLog2e : -INFINITY;
     // Rows never written by a copy must hold finite values: zero Q and KV once.
     for (uint32_t i = tid; i < (kOffP - kOffKV) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffKV)[i] = make_uint4(0, 0, 0, 0);
@@ -359,13 +357,16 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         tc::tmem_relinquish();
     }
     const bool use_cmp = a.cmp_kv != nullptr && a.Tc > 0;
-    if (warp == 0) {
-        if (lane == 0) {
-            tc::tma_prefetch_desc(&q_map);
-            tc::tma_prefetch_desc(&ori_map);
-            tc::tma_prefetch_desc(&cmp_map);
-        }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch_desc(&q_map);
+        tc::tma_prefetch_desc(&ori_map);
+        tc::tma_prefetch_desc(&cmp_map);
     }
+    // everything above is local: wait for the kernels before this one
+    grid_dependency_wait();
+    launch_dependents();
+    if (tid < 64)
+        ms->sink2[tid] = (a.sinks && tid < a.H) ? __ldg(a.sinks + tid) * kLog2e : -INFINITY;
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -1038,8 +1039,8 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     la.epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;
     la.claim_slot = (int32_t)(la.epoch % kClaimSlots);
     const int ctas = a.T < sms ? a.T : sms;
-    sparse_mla_tc_kernel<<<ctas, kThreads, kSmemBytes, stream>>>(q_map, ori_map, cmp_map, la);
-    return cudaGetLastError();
+    return launch_early(sparse_mla_tc_kernel, dim3(ctas), dim3(kThreads), kSmemBytes, stream, q_map,
+                        ori_map, cmp_map, la);
 }
 
 int32_t sparse_mla_max_topk() { return kMaxList; }
