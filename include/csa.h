@@ -416,6 +416,24 @@ csa_status_t csa_indexer_topk_noalloc(const csa_bf16_t *q, const csa_bf16_t *k, 
  */
 csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail);
 
+/*
+ * Library control, no counterpart on the pages: the limit after which a wait
+ * of the indexer and sparse-attention kernels on one of their own pipeline
+ * barriers gives up (host value, nanoseconds; 0 restores the default of 2 s).
+ * A wait that gives up records CSA_ERR_TIMEOUT in the device error word and
+ * makes its CTA stop early: it lets its copies and tensor-core operations in
+ * flight finish (those final waits keep the 2 s limit), frees its tensor
+ * memory and exits, so that the launch ends and the context stays usable; the
+ * outputs of such a launch are unspecified. A limit of a few microseconds
+ * makes normal launches give up, which is how the timeout path is tested.
+ * Applies to launches made after the call, from any host thread.
+ *
+ * The device error word's device address is looked up once per device and
+ * kept for the process: resetting a device (cudaDeviceReset) while the
+ * library is loaded is not supported.
+ */
+csa_status_t csa_set_wait_limit_ns(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

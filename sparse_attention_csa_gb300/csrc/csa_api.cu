@@ -3,6 +3,8 @@
 // documented in include/csa.h.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "csa.h"
 #include "internal.h"
@@ -41,6 +43,14 @@ csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_E
 
 namespace csa {
 int32_t *device_error_word(csa_status_t *st) { return error_word(st); }
+
+// 0: the default limit (2 s).
+std::atomic<uint64_t> g_wait_limit_ns{0};
+
+uint64_t pipeline_wait_limit_ns() {
+    const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : 2000000000ull;
+}
 }  // namespace csa
 
 extern "C" {
@@ -330,6 +340,11 @@ csa_status_t csa_compress_thd(const float *kv, const float *score, const float *
     a.hd = head_dim;
     a.overlap = overlap ? 1 : 0;
     return from_cuda(csa::launch_compress_thd(a, (cudaStream_t)stream));
+}
+
+csa_status_t csa_set_wait_limit_ns(uint64_t limit_ns) {
+    csa::g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return CSA_OK;
 }
 
 csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail) {

@@ -102,6 +102,7 @@ __device__ __forceinline__ bool bar_red_and(bool v) {
 struct Ctx {
     Misc *m;
     int32_t *err;
+    uint64_t limit;  // pipeline waits give up after this long
     __device__ __forceinline__ bool aborted() const {
         return *reinterpret_cast<volatile int32_t *>(&m->abort) != 0;
     }
@@ -111,7 +112,7 @@ struct Ctx {
     }
     __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, int site) const {
         if (aborted()) return false;
-        if (tc::mbar_wait(bar, parity)) return true;
+        if (tc::mbar_wait(bar, parity, limit)) return true;
         fail(site);
         return false;
     }
@@ -220,7 +221,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                                           ~uintptr_t(1023));
     Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Ctx cx{ms, a.err};
+    Ctx cx{ms, a.err, a.wait_ns};
     const int32_t n_groups = (a.T + kG - 1) / kG;
 
     if (tid == 0) {
@@ -660,8 +661,10 @@ size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t, int32_t, int32_t)
     return (size_t)ctas * (size_t)indexer_scratch_floats_per_cta(Tc) * sizeof(float);
 }
 
-cudaError_t launch_indexer_topk(const IndexerArgs &a, cudaStream_t stream) {
-    if (a.T == 0) return cudaSuccess;
+cudaError_t launch_indexer_topk(const IndexerArgs &args, cudaStream_t stream) {
+    if (args.T == 0) return cudaSuccess;
+    IndexerArgs a = args;
+    a.wait_ns = pipeline_wait_limit_ns();
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

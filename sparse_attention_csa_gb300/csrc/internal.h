@@ -27,6 +27,7 @@ struct IndexerArgs {
     int32_t *err;
     int32_t T, Tc, Hi, Di, batch, cmp_ratio, topk;
     int32_t max_ctas = 0;    // grid bound when > 0 (scratch sized for that many CTAs)
+    uint64_t wait_ns = 2000000000ull;  // limit of a pipeline wait (drains keep 2 s)
 };
 
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t Hi, int32_t Di, int32_t topk);
@@ -53,6 +54,7 @@ struct MlaArgs {
     float softmax_scale;
     uint32_t epoch = 0;      // set by the launcher: token-claim epoch and slot
     int32_t claim_slot = 0;
+    uint64_t wait_ns = 2000000000ull;  // limit of a pipeline wait (drains keep 2 s)
 };
 
 cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream);
@@ -121,5 +123,8 @@ cudaError_t launch_compress_thd(const CompressArgs &a, cudaStream_t stream);
 
 // Device error word of the current device (csa_api.cu).
 int32_t *device_error_word(csa_status_t *st);
+
+// Limit of the forward kernels' pipeline waits (csa_set_wait_limit_ns).
+uint64_t pipeline_wait_limit_ns();
 
 }  // namespace csa

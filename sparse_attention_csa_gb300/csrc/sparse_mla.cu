@@ -262,6 +262,7 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, bool v) {
 struct Ctx {
     Misc *m;
     int32_t *err;
+    uint64_t limit;  // pipeline waits give up after this long
     __device__ __forceinline__ bool aborted() const {
         return *reinterpret_cast<volatile int32_t *>(&m->abort) != 0;
     }
@@ -272,7 +273,7 @@ struct Ctx {
     // bounded wait; false (and abort) on timeout or when already aborted
     __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, int site) const {
         if (aborted()) return false;
-        if (tc::mbar_wait(bar, parity)) return true;
+        if (tc::mbar_wait(bar, parity, limit)) return true;
         fail(site);
         return false;
     }
@@ -329,7 +330,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                                           ~uintptr_t(1023));
     Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Ctx cx{ms, a.err};
+    Ctx cx{ms, a.err, a.wait_ns};
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
@@ -610,7 +611,8 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         bool stop = false;
         for (; !stop; ++it) {
             const uint32_t slot = it & 1;
-            if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40)) break;
+            // every lane of a loader warp takes the same decision on each wait
+            if (!__all_sync(0xffffffffu, cx.wait(&ms->info_full[slot], (it >> 1) & 1, 40))) break;
             const TokenInfo &ti = ms->info[slot];  // released after this token's loads
             if (ti.end) break;
             const int32_t *list = reinterpret_cast<const int32_t *>(smem + kOffList) + slot * kMaxList;
@@ -621,7 +623,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     // the missing rows: 16 threads per row, 256 B per slab
                     const int dr = li >> 4;
                     for (int s = 0; s < 4; ++s) {
-                        if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 44)) {
+                        if (!__all_sync(0xffffffffu, cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 44))) {
                             stop = true;
                             break;
                         }
@@ -643,7 +645,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 if (td.kind == kWinBox || td.kind == kCmpBox || ring_box(ti, td)) {
                     const CUtensorMap *map = td.kind == kCmpBox ? &cmp_map : &ori_map;
                     for (int s = 0; s < 4; ++s) {
-                        if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 41)) {
+                        if (!__all_sync(0xffffffffu, cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 41))) {
                             stop = true;
                             break;
                         }
@@ -694,7 +696,7 @@ sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 // itself once this thread's copies land; the thread goes on to
                 // the next slab without waiting.
                 for (int s = 0; s < 4; ++s) {
-                    if (!cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 42)) {
+                    if (!__all_sync(0xffffffffu, cx.wait(&ms->kv_empty[s], (kf_n & 1) ^ 1, 42))) {
                         stop = true;
                         break;
                     }
@@ -1038,6 +1040,7 @@ cudaError_t launch_sparse_mla_fwd(const MlaArgs &a, cudaStream_t stream) {
     MlaArgs la = a;
     la.epoch = epochs.fetch_add(1, std::memory_order_relaxed) + 1;
     la.claim_slot = (int32_t)(la.epoch % kClaimSlots);
+    la.wait_ns = pipeline_wait_limit_ns();
     const int ctas = a.T < sms ? a.T : sms;
     return launch_early(sparse_mla_tc_kernel, dim3(ctas), dim3(kThreads), kSmemBytes, stream, q_map,
                         ori_map, cmp_map, la);

@@ -46,16 +46,22 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 
 // Test the phase; while it is incomplete the thread may sleep (up to the
 // suspend-time hint, in ns) instead of spinning, and wakes when it completes.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity,
+                                              uint32_t hint_ns = 1000000u) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
+}
+
+// Suspend hint of a probe: 1 ms, or the wait's whole limit when that is shorter.
+__device__ __forceinline__ uint32_t probe_hint(uint64_t limit_ns) {
+    return limit_ns < 1000000ull ? (uint32_t)(limit_ns > 0 ? limit_ns : 1) : 1000000u;
 }
 
 // Wait for the phase with the given parity to complete, giving up after
@@ -63,16 +69,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // error and drains); never spins forever.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer();
+    const uint32_t hint = probe_hint(limit_ns);
+    const int probes = limit_ns < 1000000ull ? 1 : 64;  // short limits: check every probe
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < probes; ++i)
+            if (mbar_try_wait(bar, parity, hint)) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, probe_hint(limit_ns))) return true;
     return mbar_wait_slow(bar, parity, limit_ns);
 }
 

@@ -21,6 +21,9 @@ import torch
 import oracle
 from csa_inputs import packs
 
+# Lines for the terminal summary (tests/conftest.py): per-layer errors at full size.
+REPORT = []
+
 OUT_MAX_ABS = 2e-2
 OUT_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
@@ -152,3 +155,15 @@ def oracle_attention(case, idx_rows, tokens=None):
     return oracle.sparse_mla_fwd(q, t["ori_kv"], t["cmp_kv"], idx_rows, case.cu, case.cuc,
                                  case.T, t["sinks"], case.spec.scale, case.layer.cmp_ratio,
                                  case.spec.win_left, tokens=tokens)
+
+
+def indices_for_oracle(case, gpu_idx_np, tokens=None):
+    """Oracle top-k rows, replaced by the GPU's rows where they differ by a
+    near-tie (the attention is then compared with the GPU's rows)."""
+    ref = oracle_topk(case, tokens)
+    sel = gpu_idx_np if tokens is None else gpu_idx_np[tokens]
+    allowed = check_topk(case, sel, ref, tokens=tokens)
+    rows = ref[0].copy()
+    for i in allowed:
+        rows[i] = sel[i]
+    return rows

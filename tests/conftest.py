@@ -15,3 +15,13 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+def pytest_terminal_summary(terminalreporter):
+    # lines the parity tests report (per-layer errors at full size), printed
+    # after the run even in quiet mode
+    from tests._util import REPORT
+    if REPORT:
+        terminalreporter.write_sep("-", "parity report")
+        for line in REPORT:
+            terminalreporter.write_line(line)

@@ -94,3 +94,35 @@ def test_full_size_sampled(name):
             np.int32)
     ref = oracle_topk(case, toks)
     check_topk(case, idx[toks], ref, tokens=toks, gpu_val=val[toks])
+
+
+@pytest.mark.parametrize("entry", ["workspace", "noalloc"])
+@pytest.mark.parametrize("return_value", [True, False])
+def test_spill_path_against_oracle(entry, return_value):
+    """One 24,576-token sequence at ratio 4 (6,144 compressed rows): its late
+    tokens see more rows than the kernel keeps in shared memory, so their
+    scores go through the global scratch (the caller's workspace, or the
+    library's own array for the no-allocation entry point)."""
+    T, K = 24576, 512
+    layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=K, index_heads=64, index_dim=128)
+    case = layer_cases(custom_spec([T], heads=4, layers=(layer,), seed=97))[0]
+    assert case.Tc == T // 4
+    # more rows than shared memory keeps: the ordinary entry point wants a workspace
+    assert csa.csa_indexer_topk_workspace_size(T, case.Tc, 64, 128, K) > 0
+    d = case.d
+    cuc = csa.csa_compress_cu_seqlens(case.cu_d, 4)
+    call = csa.csa_indexer_topk if entry == "workspace" else csa.csa_indexer_topk_noalloc
+    idx, val = call(d["q_idx"], d["k_idx"], d["w"], case.cu_d, cuc, 4, K,
+                    return_value=return_value)
+    torch.cuda.synchronize()
+    assert csa.csa_device_error()[0] == 0
+    rng = np.random.default_rng(5)
+    late = rng.integers(5120 * 4 - 1, T, size=40)  # positions that see > 5120 rows
+    toks = np.unique(np.concatenate([late, [T - 1, 20478, 20479, 20480, 2051, 7, 0]]))
+    toks = toks.astype(np.int32)
+    ref = oracle_topk(case, toks)
+    gi = idx.cpu().numpy()[toks]
+    gv = val.cpu().numpy()[toks] if return_value else None
+    check_topk(case, gi, ref, tokens=toks, gpu_val=gv)
+    # every scored late token keeps K distinct rows of its own sequence, ascending
+    assert (gi[toks >= 20480] >= 0).all()

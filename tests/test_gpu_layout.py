@@ -27,7 +27,7 @@ def dev(a):
 EDGE = [0, 1, 3, 4, 5, 0, 7, 8, 127, 128, 129, 255, 256, 257, 2]
 
 
-@pytest.mark.parametrize("r", [2, 3, 4, 128])
+@pytest.mark.parametrize("r", [1, 2, 3, 4, 128])
 def test_compress_edge_and_random(r):
     rng = np.random.default_rng(r)
     for lengths in (EDGE, rng.integers(0, 600, size=40).tolist(), [100, 37, 119], [16384]):

@@ -9,8 +9,8 @@ import torch
 import sparse_attention_csa_gb300 as csa
 from csa_inputs import packs
 from sparse_attention_csa_gb300 import build as csa_build
-from tests._util import (check_attention, check_topk, custom_spec, layer_cases, oracle_attention,
-                         oracle_topk, sample_tokens)
+from tests._util import (check_attention, custom_spec, indices_for_oracle, layer_cases,
+                         oracle_attention, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,17 +40,6 @@ def gpu_topk(case):
     idx, _ = csa.csa_indexer_topk(d["q_idx"], d["k_idx"], d["w"], case.cu_d, cuc,
                                   case.layer.cmp_ratio, case.layer.topk)
     return idx
-
-
-def indices_for_oracle(case, gpu_idx_np, tokens=None):
-    """Oracle top-k rows, replaced by the GPU's rows where they differ by a near-tie."""
-    ref = oracle_topk(case, tokens)
-    allowed = check_topk(case, gpu_idx_np if tokens is None else gpu_idx_np[tokens], ref,
-                         tokens=tokens)
-    rows = ref[0].copy()
-    for i in allowed:
-        rows[i] = (gpu_idx_np if tokens is None else gpu_idx_np[tokens])[i]
-    return rows
 
 
 def test_tiny_pack_full():
@@ -197,3 +186,27 @@ def test_many_short_sequences():
     out, lse = gpu_attention(case, idx)
     ref_out, ref_lse = oracle_attention(case, rows)
     check_attention(out, lse, ref_out, ref_lse, "700 sequences")
+
+
+def test_no_compress_ratio_one():
+    """NO_COMPRESS: the compressor gives no rows and the ratio is 1; the
+    attention is the window alone (with sinks)."""
+    import oracle
+    lengths = [300, 1, 129, 57]
+    layer = packs.LayerSpec(cmp_ratio=1, indexer=False)
+    case = layer_cases(custom_spec(lengths, heads=16, win_left=127, layers=(layer,)))[0]
+    cuc = csa.csa_compress_cu_seqlens(case.cu_d, 1)
+    np.testing.assert_array_equal(cuc.cpu().numpy(), case.cu)  # ratio 1: every token a row
+    d = case.d
+    out, lse = csa.csa_sparse_mla_fwd(d["q"], d["ori_kv"], None, None, case.cu_d, case.cu_d, cuc,
+                                      d["sinks"], case.spec.scale, 1, 127,
+                                      return_softmax_lse=True)
+    ref_out, ref_lse = oracle.sparse_mla_fwd(case.t["q"], case.t["ori_kv"], None, None, case.cu,
+                                             case.cu, case.T, case.t["sinks"], case.spec.scale,
+                                             1, 127)
+    check_attention(out, lse, ref_out, ref_lse, "ratio 1, window only")
+    # compressed rows at ratio 1 are not an accepted request
+    with pytest.raises(csa.CsaError) as e:
+        csa.csa_sparse_mla_fwd(d["q"], d["ori_kv"], d["ori_kv"], None, case.cu_d, case.cu_d, cuc,
+                               d["sinks"], case.spec.scale, 1, 127)
+    assert e.value.code == 3  # CSA_ERR_UNSUPPORTED

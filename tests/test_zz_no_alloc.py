@@ -9,11 +9,13 @@ takes. It uses the library's own fixed-size scratch array instead.
 The pack here is one sequence long enough that its late tokens see more
 compressed rows than the kernel keeps in shared memory, so their scores go
 through the scratch. Two calls in a row must both give what the ordinary
-entry point gives with a workspace from the caller. This file is named to be
+entry point gives with a workspace from the caller, and sampled tokens of
+both must follow the fp64 oracle's top-k rule. This file is named to be
 collected last.
 """
 
 import ctypes as C
+from types import SimpleNamespace
 
 import numpy as np
 import pytest
@@ -21,7 +23,7 @@ import torch
 
 import sparse_attention_csa_gb300 as csa
 from sparse_attention_csa_gb300 import build as csa_build
-from tests._util import VAL_ATOL, VAL_RTOL
+from tests._util import VAL_ATOL, VAL_RTOL, check_topk, oracle_topk
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +53,16 @@ def test_noalloc_matches_workspace_entry_point():
     assert csa.csa_device_error()[0] == 0
     # the last token sees every row and keeps the 16 best of 42,500
     assert (ref_idx[-1] >= 0).all() and ref_idx[-1].unique().numel() == K
+    # and both agree with the fp64 oracle on sampled tokens, late ones included
+    case = SimpleNamespace(
+        t={"q_idx": q.cpu(), "k_idx": k.cpu(), "w": w.cpu()}, T=T, cu=np.array([0, T], np.int32),
+        cuc=np.array([0, T // r], np.int32),
+        layer=SimpleNamespace(cmp_ratio=r, topk=K))
+    rng = np.random.default_rng(11)
+    toks = np.unique(np.concatenate([rng.integers(5120 * r, T, size=32), [T - 1, 3, 100]]))
+    toks = toks.astype(np.int32)
+    ref = oracle_topk(case, toks)
+    check_topk(case, idx.cpu().numpy()[toks], ref, tokens=toks, gpu_val=val.cpu().numpy()[toks])
 
 
 def test_noalloc_rejects_more_rows_than_the_scratch_holds():
