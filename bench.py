@@ -306,21 +306,32 @@ def oracle_inputs(layers):
     return out
 
 
-def oracle_step(layers, prepared, tokens):
-    """The whole path for the listed tokens through the fp64 oracle."""
+def oracle_step(layers, prepared, tokens, stages=None):
+    """The whole path for the listed tokens through the fp64 oracle; adds each
+    stage's seconds to ``stages`` (A1 compressed cu_seqlens, A2 window rows,
+    A3+A4 indexer and top-k, A6 sparse attention) when given."""
     import oracle
     tk = torch.from_numpy(tokens).long()
+
+    def timed(name, fn):
+        t0 = time.perf_counter()
+        r = fn()
+        if stages is not None:
+            stages[name] = stages.get(name, 0.0) + time.perf_counter() - t0
+        return r
+
     for L, d in zip(layers, prepared):
         spec, layer, h = L.spec, L.layer, L.host
-        cuc = oracle.compress_cu_seqlens(d["cu"], layer.cmp_ratio)
+        cuc = timed("A1", lambda: oracle.compress_cu_seqlens(d["cu"], layer.cmp_ratio))
+        timed("A2", lambda: oracle.window_idx(d["cu"], spec.total_tokens, spec.win_left, tokens))
         idx = None
         if layer.indexer:
-            idx, *_ = oracle.indexer_topk(h["q_idx"][tk], d["k_idx"], h["w"][tk],
-                                          spec.total_tokens, d["cu"], cuc, layer.cmp_ratio,
-                                          layer.topk, tokens=tokens)
-        oracle.sparse_mla_fwd(h["q"][tk], d["ori_kv"], d["cmp_kv"], idx, d["cu"], cuc,
-                              spec.total_tokens, d["sinks"], spec.scale, layer.cmp_ratio,
-                              spec.win_left, tokens=tokens)
+            idx = timed("A3+A4", lambda: oracle.indexer_topk(
+                h["q_idx"][tk], d["k_idx"], h["w"][tk], spec.total_tokens, d["cu"], cuc,
+                layer.cmp_ratio, layer.topk, tokens=tokens)[0])
+        timed("A6", lambda: oracle.sparse_mla_fwd(
+            h["q"][tk], d["ori_kv"], d["cmp_kv"], idx, d["cu"], cuc, spec.total_tokens,
+            d["sinks"], spec.scale, layer.cmp_ratio, spec.win_left, tokens=tokens))
 
 
 def token_sample(T, n, offset):
@@ -328,22 +339,53 @@ def token_sample(T, n, offset):
     return ((np.arange(n, dtype=np.int64) * stride + offset) % T).astype(np.int32)
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), else what the platform reports."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(layers, seconds):
+    """The fp64 oracle on evenly spaced tokens of the pack: all host threads for
+    about ``seconds``, then one thread for a quarter of that; per-stage times
+    from the all-thread run."""
     import oracle
     prepared = oracle_inputs(layers)
     T = layers[0].spec.total_tokens
-    done, batch, off = 0, 64, 0
-    t0 = time.perf_counter()
-    while True:
-        oracle_step(layers, prepared, token_sample(T, batch, off))
-        done += batch
-        off += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or done >= T:
-            break
-    return {"value": done / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+
+    def run(budget, stages=None):
+        done, batch, off = 0, 64, 0
+        t0 = time.perf_counter()
+        while True:
+            oracle_step(layers, prepared, token_sample(T, batch, off), stages)
+            done += batch
+            off += 1
+            el = time.perf_counter() - t0
+            if el >= budget or done >= T:
+                return done, el
+
+    threads = oracle.num_threads()
+    stages = {}
+    done, el = run(seconds, stages)
+    oracle.set_num_threads(1)
+    try:
+        done1, el1 = run(seconds / 4)
+    finally:
+        oracle.set_num_threads(threads)
+    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{done} tokens of the {layers[0].spec.name} pack (evenly spaced), "
-                      f"all layers, fp64 C oracle, {el:.1f} s"}
+                      f"all layers, fp64 C oracle, {el:.1f} s on {threads} threads",
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+            "single_thread": {"value": done1 / el1, "unit": UNIT, "tokens": done1,
+                              "seconds": round(el1, 2)},
+            "stage_ms_per_1k_tokens": {k: 1e6 * v / done for k, v in stages.items()}}
 
 
 # --------------------------------------------------------------------------- arms
@@ -709,18 +751,43 @@ def run_e2e(args, layers, stream, flush, world, device):
         d2h += sum(t.numel() * t.element_size() for t in outs.values())
         pinned_out.append(outs)
 
-    def step():
+    # Three streams: inputs copied in on one, the layers on the compute stream,
+    # outputs copied out on a third. Layer 2's inputs load while layer 1 runs,
+    # each layer's outputs leave as soon as it is done, and copies in and out
+    # overlap (the link is full duplex). A step starts and ends on the compute
+    # stream; its events bracket every copy and kernel of the step.
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+
+    def step(start, end):
         n = 0
-        for L, ins, outs in zip(layers, pinned_in, pinned_out):
-            for k, p in ins.items():
-                L.dev[k].copy_(p, non_blocking=True)
+        s_in.wait_event(start)
+        loaded = []
+        for L, ins in zip(layers, pinned_in):
+            with torch.cuda.stream(s_in):
+                for k, p in ins.items():
+                    L.dev[k].copy_(p, non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_in)
+            loaded.append(e)
+        for L, outs, e in zip(layers, pinned_out, loaded):
+            stream.wait_event(e)
             n += L.launches(stream)
-            outs["out"].copy_(L.out, non_blocking=True)
-            outs["lse"].copy_(L.lse, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(stream)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                outs["out"].copy_(L.out, non_blocking=True)
+                outs["lse"].copy_(L.lse, non_blocking=True)
+        fin = torch.cuda.Event()
+        fin.record(s_out)
+        stream.wait_event(fin)
+        end.record(stream)
         return n
 
     for _ in range(max(1, args.warmup)):
-        step()
+        a, b = torch.cuda.Event(), torch.cuda.Event()
+        a.record(stream)
+        step(a, b)
     torch.cuda.synchronize()
     times = []
     barrier(world)
@@ -728,8 +795,7 @@ def run_e2e(args, layers, stream, flush, world, device):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step()
-        b.record(stream)
+        step(a, b)
         times.append((a, b))
     torch.cuda.synchronize()
     barrier(world)

@@ -30,8 +30,11 @@ def lib():
         f64p = C.POINTER(C.c_double)
         i32 = C.c_int32
         _lib.csa_ref_num_threads.restype = C.c_int
+        _lib.csa_ref_set_num_threads.argtypes = [C.c_int]
+        _lib.csa_ref_set_num_threads.restype = None
         _lib.csa_ref_compress_cu_seqlens.argtypes = [i32p, i32, i32, i32p]
         _lib.csa_ref_window_idx.argtypes = [i32p, i32, i32, i32, i32p]
+        _lib.csa_ref_window_idx_tokens.argtypes = [i32p, i32, i32, i32, i32p, i32, i32p]
         _lib.csa_ref_indexer_topk.argtypes = [
             f64p, f64p, f64p, i32, i32, i32, i32, i32p, i32p, i32, i32, i32, i32p, i32,
             i32p, f64p, f64p, f64p, i32p]
@@ -46,7 +49,7 @@ def lib():
             C.c_double, i32p, i32, f64p, f64p, f64p, f64p, f64p]
         _lib.csa_ref_compress_thd.argtypes = [
             f64p, f64p, f64p, i32p, i32p, i32, i32, i32, i32, i32, f64p]
-        for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx",
+        for name in ("csa_ref_compress_cu_seqlens", "csa_ref_window_idx", "csa_ref_window_idx_tokens",
                      "csa_ref_indexer_topk", "csa_ref_sparse_mla_fwd", "csa_ref_sparse_mla_bwd",
                      "csa_ref_indexer_kl_loss_grad", "csa_ref_compress_thd"):
             getattr(_lib, name).restype = C.c_int
@@ -80,6 +83,12 @@ def num_threads() -> int:
     return int(lib().csa_ref_num_threads())
 
 
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (n < 1: one per
+    processor)."""
+    lib().csa_ref_set_num_threads(int(n))
+
+
 def compress_cu_seqlens(cu_seqlens, cmp_ratio: int) -> np.ndarray:
     cu = _i32(cu_seqlens)
     out = np.zeros_like(cu)
@@ -88,8 +97,16 @@ def compress_cu_seqlens(cu_seqlens, cmp_ratio: int) -> np.ndarray:
     return out
 
 
-def window_idx(cu_seqlens, total_tokens: int, ori_win_left: int) -> np.ndarray:
+def window_idx(cu_seqlens, total_tokens: int, ori_win_left: int, tokens=None) -> np.ndarray:
+    """Window rows of every token ([T, W]), or of the listed tokens only."""
     cu = _i32(cu_seqlens)
+    if tokens is not None:
+        tok = _i32(tokens)
+        out = np.zeros((len(tok), ori_win_left + 1), dtype=np.int32)
+        _check(lib().csa_ref_window_idx_tokens(_p(cu, C.c_int32), len(cu) - 1, total_tokens,
+                                               ori_win_left, _p(tok, C.c_int32), len(tok),
+                                               _p(out, C.c_int32)), "window_idx")
+        return out
     out = np.zeros((total_tokens, ori_win_left + 1), dtype=np.int32)
     _check(lib().csa_ref_window_idx(_p(cu, C.c_int32), len(cu) - 1, total_tokens, ori_win_left,
                                     _p(out, C.c_int32)), "window_idx")

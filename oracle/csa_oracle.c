@@ -48,6 +48,15 @@ int csa_ref_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops from now on (n < 1: one per processor). */
+void csa_ref_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 /* cu_seqlens must start at 0 and never decrease. */
 static int check_cu(const int32_t *cu, int32_t batch, int64_t total) {
     if (!cu || batch < 0) return 0;
@@ -97,20 +106,39 @@ int csa_ref_compress_cu_seqlens(const int32_t *cu_seqlens, int32_t batch, int32_
  * RFC, section 2, has ori_win_left=127, ori_win_right=0: 127 rows to the left
  * plus the token itself).
  */
+static void window_row(const int32_t *cu_seqlens, int32_t batch, int32_t t, int32_t W,
+                       int32_t *row_out) {
+    int32_t b = segment_of(cu_seqlens, batch, t);
+    int32_t seg_start = cu_seqlens[b];
+    int32_t start = t - W + 1;
+    if (start < seg_start) start = seg_start;
+    for (int32_t i = 0; i < W; ++i) {
+        int32_t row = start + i;
+        row_out[i] = (row > t) ? -1 : row;
+    }
+}
+
 int csa_ref_window_idx(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
                        int32_t ori_win_left, int32_t *idx) {
     if (!cu_seqlens || !idx || batch < 0 || total_tokens < 0 || ori_win_left < 0) return REF_ERR_ARG;
     if (!check_cu(cu_seqlens, batch, total_tokens)) return REF_ERR_ARG;
     const int32_t W = ori_win_left + 1;
-    for (int32_t t = 0; t < total_tokens; ++t) {
-        int32_t b = segment_of(cu_seqlens, batch, t);
-        int32_t seg_start = cu_seqlens[b];
-        int32_t start = t - W + 1;
-        if (start < seg_start) start = seg_start;
-        for (int32_t i = 0; i < W; ++i) {
-            int32_t row = start + i;
-            idx[(int64_t)t * W + i] = (row > t) ? -1 : row;
-        }
+    for (int32_t t = 0; t < total_tokens; ++t) window_row(cu_seqlens, batch, t, W, idx + (int64_t)t * W);
+    return REF_OK;
+}
+
+/* The same rows for the listed tokens only: row i of idx for tokens[i]. */
+int csa_ref_window_idx_tokens(const int32_t *cu_seqlens, int32_t batch, int32_t total_tokens,
+                              int32_t ori_win_left, const int32_t *tokens, int32_t n_tokens,
+                              int32_t *idx) {
+    if (!cu_seqlens || !idx || !tokens || batch < 0 || total_tokens < 0 || ori_win_left < 0 ||
+        n_tokens < 0)
+        return REF_ERR_ARG;
+    if (!check_cu(cu_seqlens, batch, total_tokens)) return REF_ERR_ARG;
+    const int32_t W = ori_win_left + 1;
+    for (int32_t i = 0; i < n_tokens; ++i) {
+        if (tokens[i] < 0 || tokens[i] >= total_tokens) return REF_ERR_ARG;
+        window_row(cu_seqlens, batch, tokens[i], W, idx + (int64_t)i * W);
     }
     return REF_OK;
 }

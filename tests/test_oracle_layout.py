@@ -125,3 +125,13 @@ def test_visible_blocks_golden():
         assert len(rows) == count, t
         if count:
             assert rows[0] == first and rows[-1] == last, t
+
+
+def test_window_rows_of_listed_tokens_match_the_whole_table():
+    rng = np.random.default_rng(3)
+    cu = np.concatenate([[0], np.cumsum(rng.integers(1, 300, size=9))]).astype(np.int32)
+    T = int(cu[-1])
+    toks = rng.integers(0, T, size=50).astype(np.int32)
+    for W in (1, 16, 128):
+        whole = oracle.window_idx(cu, T, W - 1)
+        np.testing.assert_array_equal(oracle.window_idx(cu, T, W - 1, toks), whole[toks])
