@@ -190,6 +190,8 @@ class Layer:
                                                        layer.index_dim, layer.topk)
             self.ws = torch.empty(need, dtype=torch.uint8, device=device) if need else None
         self.acc = layer_accounting(spec, layer)
+        self.side = torch.cuda.Stream(device=device)
+        self.win_done = torch.cuda.Event()
 
     def launches(self, stream, events=None, names=None, per_kernel=True):
         """Run the layer; optionally record an event after each launch
@@ -208,10 +210,20 @@ class Layer:
         csa.csa_compress_cu_seqlens(d["cu"], L.cmp_ratio, out=self.cuc, stream=stream)
         n += 1
         mark(f"compress_cu_seqlens/r{L.cmp_ratio}")
-        csa.csa_window_idx(d["cu"], spec.total_tokens, spec.win_left, 0, out=self.win,
-                           stream=stream)
+        if per_kernel:
+            csa.csa_window_idx(d["cu"], spec.total_tokens, spec.win_left, 0, out=self.win,
+                               stream=stream)
+            mark(f"window_idx/r{L.cmp_ratio}")
+        else:
+            # the window rows depend on nothing else of the layer: on a side
+            # stream, beside the indexer, joined before the layer ends
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            self.side.wait_event(fork)
+            csa.csa_window_idx(d["cu"], spec.total_tokens, spec.win_left, 0, out=self.win,
+                               stream=self.side)
+            self.win_done.record(self.side)
         n += 1
-        mark(f"window_idx/r{L.cmp_ratio}")
         idx = None
         if L.indexer:
             idx, _ = csa.csa_indexer_topk(d["q_idx"], d["k_idx"], d["w"], d["cu"], self.cuc,
@@ -223,6 +235,8 @@ class Layer:
                                d["sinks"], spec.scale, L.cmp_ratio, spec.win_left, 0, True,
                                out=self.out, lse=self.lse, stream=stream)
         n += 1
+        if not per_kernel:
+            stream.wait_event(self.win_done)
         mark(f"sparse_mla_fwd/r{L.cmp_ratio}" if per_kernel else f"layer/r{L.cmp_ratio}", last=True)
         return n
 

@@ -109,10 +109,11 @@ cudaError_t launch_window_idx(const int32_t *cu, int32_t batch, int32_t total_to
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // about four tokens per warp, at most eight 256-thread blocks per SM
+    // One 256-thread block per SM at most (runs of tokens per warp): the
+    // blocks then fit beside a concurrent indexer or attention CTA.
     const int warps_per_block = 8;
     int64_t blocks = ((int64_t)total_tokens + 4 * warps_per_block - 1) / (4 * warps_per_block);
-    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    if (blocks > (int64_t)sms) blocks = (int64_t)sms;
     const bool vec4 = (window & 3) == 0 && ((uintptr_t)idx & 15u) == 0;
     return launch_early(window_idx_kernel, dim3((unsigned)blocks), dim3(32 * warps_per_block), 0,
                         stream, cu, batch, total_tokens, window, vec4, idx, err);

@@ -11,7 +11,8 @@ rows plus the selected compressed rows):
 4. ``csa_sparse_mla_fwd``       attention with sinks (COMPRESSOR_ONLY layers
                                 attend every visible compressed row).
 
-Everything runs on the current CUDA stream; nothing synchronises.
+Everything runs on the current CUDA stream (the window rows optionally on a
+side stream, joined before returning); nothing synchronises.
 """
 
 from __future__ import annotations
@@ -47,10 +48,14 @@ def allocate_outputs(T, H, D, W, topk, batch, device, with_window=True, with_lse
 def csa_layer_forward(q, ori_kv, cmp_kv, cu_seqlens, sinks, softmax_scale: float, cmp_ratio: int,
                       ori_win_left: int, q_idx=None, k_idx=None, w=None, topk: int = 0,
                       return_softmax_lse: bool = True, with_window: bool = True,
-                      outputs: LayerOutputs | None = None, workspace=None) -> LayerOutputs:
+                      outputs: LayerOutputs | None = None, workspace=None,
+                      window_stream=None) -> LayerOutputs:
     """Forward of one layer. ``q_idx``/``k_idx``/``w``/``topk`` given -> INDEXER
     layer (CSA); omitted -> COMPRESSOR_ONLY layer (HCA, every visible block).
-    ``cmp_kv`` must hold exactly the pack's compressed row count."""
+    ``cmp_kv`` must hold exactly the pack's compressed row count.
+    ``window_stream`` (a CUDA stream): the window rows, which nothing else of
+    the layer reads, are computed there, beside the indexer, and the current
+    stream waits for them before returning."""
     T, H, D = q.shape
     batch = cu_seqlens.numel() - 1
     indexer = q_idx is not None
@@ -58,8 +63,17 @@ def csa_layer_forward(q, ori_kv, cmp_kv, cu_seqlens, sinks, softmax_scale: float
         outputs = allocate_outputs(T, H, D, ori_win_left + 1, topk if indexer else 0, batch,
                                    q.device, with_window, return_softmax_lse)
     csa_compress_cu_seqlens(cu_seqlens, cmp_ratio, out=outputs.cu_seqlens_cmp)
+    main = torch.cuda.current_stream()
+    win_done = None
     if with_window:
-        csa_window_idx(cu_seqlens, T, ori_win_left, 0, out=outputs.window_idx)
+        if window_stream is None:
+            csa_window_idx(cu_seqlens, T, ori_win_left, 0, out=outputs.window_idx)
+        else:
+            window_stream.wait_stream(main)
+            csa_window_idx(cu_seqlens, T, ori_win_left, 0, out=outputs.window_idx,
+                           stream=window_stream)
+            win_done = torch.cuda.Event()
+            win_done.record(window_stream)
     idx = None
     if indexer:
         if workspace is None:
@@ -71,4 +85,6 @@ def csa_layer_forward(q, ori_kv, cmp_kv, cu_seqlens, sinks, softmax_scale: float
     csa_sparse_mla_fwd(q, ori_kv, cmp_kv, idx, cu_seqlens, cu_seqlens, outputs.cu_seqlens_cmp,
                        sinks, softmax_scale, cmp_ratio, ori_win_left, 0, return_softmax_lse,
                        out=outputs.out, lse=outputs.lse)
+    if win_done is not None:
+        main.wait_event(win_done)
     return outputs
