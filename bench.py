@@ -10,8 +10,9 @@ window 128, per-head sinks. Inputs are synthetic (seeded N(0,1)).
 
 One step = the whole path for both layers: compressed cu_seqlens, window
 rows, indexer + top-k (CSA layer), sparse MLA with sinks. Inputs are resident
-in HBM when the timed region starts; L2 is flushed (a 256 MB write) between
-steps, outside the per-step CUDA events. ``value`` is tokens / device time.
+in HBM when the timed region starts; L2 is flushed between steps (a 256 MB
+write, then a 256 MB read that evicts the write's dirty lines), outside the
+per-step CUDA events. ``value`` is tokens / device time.
 The timed steps record events only before each step and after each layer (the
 kernels of a layer are launched back to back, each allowed to start while the
 one before it finishes); per-kernel times come from separate steps after the
@@ -83,6 +84,9 @@ def parse_args():
     p.add_argument("--cmp", action="store_true",
                    help="also time the THD compressor core for each layer's ratio "
                         "(one more JSON line)")
+    p.add_argument("--cmp-only", action="store_true",
+                   help="time only the THD compressor core (its own inputs; the forward "
+                        "layers' tensors are not allocated) and print its line alone")
     p.add_argument("--kl", action="store_true",
                    help="also time the indexer KL-loss gradient of each indexer layer "
                         "(one more JSON line)")
@@ -239,6 +243,21 @@ class Layer:
             stream.wait_event(self.win_done)
         mark(f"sparse_mla_fwd/r{L.cmp_ratio}" if per_kernel else f"layer/r{L.cmp_ratio}", last=True)
         return n
+
+
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2, then read another
+    one, so that the next step starts with L2 holding none of its inputs and
+    no dirty lines (the write's lines are written back while the read evicts
+    them, not while the timed kernels run). Both run outside the step events."""
+
+    def __init__(self, device):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
 
 
 def build_layers(spec, device):
@@ -428,7 +447,7 @@ def run_ours(args, world, rank, local):
     spec = packs.pack_spec(args.config)
     layers = build_layers(spec, device)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     T = spec.total_tokens
 
     import sparse_attention_csa_gb300 as csa
@@ -437,7 +456,7 @@ def run_ours(args, world, rank, local):
         return sum(L.launches(stream, events, names, per_kernel) for L in layers)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     st, word = csa.csa_device_error()
@@ -456,7 +475,7 @@ def run_ours(args, world, rank, local):
     # kernel may then start while the one before it finishes).
     recs = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         ev = [torch.cuda.Event(enable_timing=True)]
         ev[0].record(stream)
         nm = []
@@ -477,7 +496,7 @@ def run_ours(args, world, rank, local):
     # Per-kernel breakdown (dominant kernel, kernels_ms): separate steps with an
     # event after every launch, after the timed region.
     for _ in range(max(3, min(args.steps, 10))):
-        flush.zero_()
+        flush()
         ev = [torch.cuda.Event(enable_timing=True)]
         ev[0].record(stream)
         nm = []
@@ -537,7 +556,8 @@ def run_ours(args, world, rank, local):
                                    for l in spec.layers)
                                + f", H={spec.heads}, D={spec.dim}, window {spec.win_left + 1}",
                    "tokens_per_step": T, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed between steps (256 MB write, outside the step events)",
+                   "l2": "flushed between steps (256 MB write, then a 256 MB read that "
+                         "evicts its dirty lines; outside the step events)",
                    "timing": "events at step and layer boundaries; per-kernel times from "
                              "separate steps with an event after every launch",
                    "indexer_values": "not requested: tokens whose visible blocks fit in top-k "
@@ -563,12 +583,35 @@ def run_ours(args, world, rank, local):
     return result
 
 
+class CmpLayer:
+    """A layer's compressed-row offsets alone, for the compressor-only run."""
+
+    def __init__(self, spec, layer, device):
+        import sparse_attention_csa_gb300 as csa
+        self.spec, self.layer = spec, layer
+        cu = np.concatenate([[0], np.cumsum(spec.lengths)]).astype(np.int32)
+        self.cu = torch.from_numpy(cu).to(device)
+        self.cuc = csa.csa_compress_cu_seqlens(self.cu, layer.cmp_ratio)
+        self.Tc = int(self.cuc[-1].item())
+
+
+def run_cmp_only(args):
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    spec = packs.pack_spec(args.config)
+    layers = [CmpLayer(spec, layer, device) for layer in spec.layers]
+    flush = L2Flush(device)
+    peaks, peak_kind = load_peaks()
+    return run_cmp(args, layers, torch.cuda.current_stream(), flush, peaks, peak_kind)
+
+
 def run_cmp(args, layers, stream, flush, peaks, peak_src):
     """The THD compressor core for each layer's ratio on this pack (head_dim
     512, overlap, position embedding), from seeded N(0,1) projections drawn
     on the device, timed per launch with CUDA events between L2 flushes.
-    Algorithmic bytes: every grouped row of both projections read once
-    (2 x 1024 fp32 each), the position embedding and the fp32 output."""
+    Algorithmic bytes: every half row the overlap transform uses, read once
+    from both projections (512 fp32 each), the position embedding and the
+    fp32 output."""
     import sparse_attention_csa_gb300 as csa
     spec = layers[0].spec
     T, hd = spec.total_tokens, 512
@@ -588,11 +631,11 @@ def run_cmp(args, layers, stream, flush, peaks, peak_src):
 
         csa.csa_compress_cu_seqlens(L.cu, r, out=L.cuc, stream=stream)
         for _ in range(3):
-            flush.zero_()
+            flush()
             call()
         ms = []
         for _ in range(max(args.bwd_steps, 5)):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             call()
@@ -600,8 +643,13 @@ def run_cmp(args, layers, stream, flush, peaks, peak_src):
             torch.cuda.synchronize()
             ms.append(a.elapsed_time(b))
         per[f"compress_thd/r{r}"] = statistics.median(ms)
-        grouped = L.Tc * r
-        nbytes += 2 * grouped * 2 * hd * 4 + r * 2 * hd * 4 + L.Tc * hd * 4
+        # every group reads the second halves of its own r rows and, unless it
+        # is its sequence's first, the first halves of the previous group's
+        # rows, in both projections; plus the position embedding and the output
+        cuc = L.cuc.cpu().numpy()
+        firsts = int(np.count_nonzero(cuc[1:] > cuc[:-1]))
+        halves = L.Tc * r + (L.Tc - firsts) * r
+        nbytes += halves * 2 * hd * 4 + r * 2 * hd * 4 + L.Tc * hd * 4
     st, word = csa.csa_device_error()
     if st != 0:
         raise RuntimeError(f"device error in the compressor: {word:#x}")
@@ -613,7 +661,8 @@ def run_cmp(args, layers, stream, flush, peaks, peak_src):
         "steps": max(args.bwd_steps, 5), "warmup": 3, "ms_per_step": total,
         "higher_is_better": True, "dtype": "f32", "data": "synthetic", "part": "compressor",
         "config": {"workload": f"{spec.name}, one compressor per layer ratio, head_dim 512, "
-                               "overlap, projections given", "l2": "flushed between launches"},
+                               "overlap, projections given",
+                   "l2": "flushed between launches (256 MB write, then 256 MB read)"},
         "kernels_ms": per,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -658,11 +707,11 @@ def run_kl(args, layers, stream, flush):
                                                 stream=stream)
 
         for _ in range(2):
-            flush.zero_()
+            flush()
             call()
         ms = []
         for _ in range(args.bwd_steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             call()
@@ -687,7 +736,7 @@ def run_kl(args, layers, stream, flush):
         "dtype": "f32 (CUDA cores, from bf16 inputs)", "data": "synthetic", "part": "indexer KL",
         "config": {"workload": f"{spec.name}, indexer layers, own top-k rows, attention "
                                "distribution as target", "list_entries": entries,
-                   "l2": "flushed between launches"},
+                   "l2": "flushed between launches (256 MB write, then 256 MB read)"},
         "kernels_ms": per,
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": how, "flops": flops},
@@ -715,11 +764,11 @@ def run_bwd(args, layers, stream, flush, peaks, peak_src):
                                           stream=stream)
 
         for _ in range(2):
-            flush.zero_()
+            flush()
             call()
         ms = []
         for _ in range(args.bwd_steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             call()
@@ -740,7 +789,7 @@ def run_bwd(args, layers, stream, flush, peaks, peak_src):
         "steps": args.bwd_steps, "warmup": 2, "ms_per_step": total, "higher_is_better": True,
         "dtype": "bf16 (tcgen05, fp32 accumulate)", "data": "synthetic", "part": "backward",
         "config": {"workload": f"{spec.name}, every layer, forward out/lse as inputs",
-                   "l2": "flushed between launches"},
+                   "l2": "flushed between launches (256 MB write, then 256 MB read)"},
         "kernels_ms": per,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
@@ -806,7 +855,7 @@ def run_e2e(args, layers, stream, flush, world, device):
     times = []
     barrier(world)
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         step(a, b)
@@ -873,6 +922,9 @@ def main():
         res = run_reference(args, world, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+    if args.cmp_only:
+        print(json.dumps(run_cmp_only(args)), flush=True)
         return
     world, rank, local = dist_setup("nccl")
     res = run_ours(args, world, rank, local)
