@@ -577,7 +577,7 @@ def run_ours(args, world, rank, local):
     if args.bwd and rank == 0:
         result["_bwd"] = run_bwd(args, layers, stream, flush, peaks, peak_kind)
     if args.kl and rank == 0:
-        result["_kl"] = run_kl(args, layers, stream, flush)
+        result["_kl"] = run_kl(args, layers, stream, flush, peaks, peak_kind)
     if args.cmp and rank == 0:
         result["_cmp"] = run_cmp(args, layers, stream, flush, peaks, peak_kind)
     return result
@@ -670,21 +670,14 @@ def run_cmp(args, layers, stream, flush, peaks, peak_src):
     }
 
 
-def fp32_alu_peak_tflops():
-    """FP32 FMA peak of the CUDA cores from unit counts and the maximum SM
-    clock: SMs x 128 fp32 lanes x 2 FLOP per FMA x clock."""
-    peaks, _ = load_peaks()
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"{sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz"
-
-
-def run_kl(args, layers, stream, flush):
+def run_kl(args, layers, stream, flush, peaks, peak_src):
     """The indexer KL-loss gradient of each indexer layer, on that layer's own
     top-k rows with the attention backward's head-averaged distribution over
     them (cmp_softmax_l1_norm) as the target, timed per launch with CUDA
     events between L2 flushes. Algorithmic FLOPs per (token, listed row):
-    2 Hi Di each for the score, d_q and d_k -> 6 Hi Di (fp32 CUDA cores)."""
+    2 Hi Di each for the score, d_q and d_k -> 6 Hi Di; the contractions run
+    on the tensor cores (bf16 operands, fp32 accumulation), so the roofline is
+    the bf16 tensor peak."""
     import sparse_attention_csa_gb300 as csa
     gen = torch.Generator().manual_seed(8)
     per, flops, entries = {}, 0, 0
@@ -728,18 +721,19 @@ def run_kl(args, layers, stream, flush):
     total = sum(per.values())
     spec = layers[0].spec
     achieved = flops / (total * 1e-3) / 1e12
-    peak, how = fp32_alu_peak_tflops()
     return {
         "metric": "indexer KL-loss gradient tokens/s (loss, d_q, d_k, d_w) on 1 GB300",
         "value": spec.total_tokens / (total * 1e-3), "unit": UNIT, "n_gpus": 1,
         "steps": args.bwd_steps, "warmup": 2, "ms_per_step": total, "higher_is_better": True,
-        "dtype": "f32 (CUDA cores, from bf16 inputs)", "data": "synthetic", "part": "indexer KL",
+        "dtype": "bf16 (tcgen05, fp32 accumulate; G as a bf16 hi + lo pair)", "data": "synthetic",
+        "part": "indexer KL",
         "config": {"workload": f"{spec.name}, indexer layers, own top-k rows, attention "
                                "distribution as target", "list_entries": entries,
                    "l2": "flushed between launches (256 MB write, then 256 MB read)"},
         "kernels_ms": per,
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": how, "flops": flops},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": peak_src, "flops": flops},
     }
 
 

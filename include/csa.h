@@ -263,7 +263,10 @@ csa_status_t csa_sparse_mla_bwd(const csa_bf16_t *q, const csa_bf16_t *dout, con
  * Outputs, fp32, overwritten: d_q [T, Hi, Di], d_k [Tc, Di], d_w [T, Hi],
  * loss [T] (unscaled KL per token; may be NULL). d_k is a sum over tokens
  * made with fp32 atomics, so its last bits depend on the order the tokens
- * finish in.
+ * finish in. Arithmetic: with Di = 128 the contractions run on the tensor
+ * cores (bf16 q and k as given, fp32 accumulation; the per-entry factor
+ * g_s w[t,h] [a_hs > 0] enters as the sum of two bf16 parts, about 2^-17
+ * relative); with Di = 64 everything is fp32 on the CUDA cores.
  * Errors: negative sizes or topk < 1 -> CSA_ERR_SHAPE; Di not in {64, 128},
  * Hi not in [1, 64], cmp_ratio < 2, topk > 2048 -> CSA_ERR_UNSUPPORTED;
  * NULL inputs or outputs (k and d_k may be NULL only when Tc == 0) ->

@@ -31,7 +31,8 @@
 // columns per thread), which are added to d_k with 16-byte atomics (a warp
 // covers 512 contiguous bytes of one row). Every contraction reads its
 // shared operands as float4 register tiles, about one load per 5-10 FMAs.
-// All arithmetic is fp32 on the CUDA cores.
+// All arithmetic is fp32 on the CUDA cores. This kernel serves index_dim 64;
+// index_dim 128 runs on the tensor cores (indexer_kl_grad_tc.cu).
 #include "common.cuh"
 #include "internal.h"
 
@@ -402,12 +403,14 @@ cudaError_t launch_indexer_kl_grad(const IndexerKlArgs &a, cudaStream_t stream) 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    // index_dim 128: the contractions on the tensor cores
+    if (a.Di == 128) return launch_indexer_kl_grad_tc(a, stream);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    return a.Di == 128 ? launch_kl<128>(a, sms, stream) : launch_kl<64>(a, sms, stream);
+    return launch_kl<64>(a, sms, stream);
 }
 
 }  // namespace csa

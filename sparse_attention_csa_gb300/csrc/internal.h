@@ -105,6 +105,8 @@ struct IndexerKlArgs {
 };
 
 cudaError_t launch_indexer_kl_grad(const IndexerKlArgs &a, cudaStream_t stream);
+// The tensor-core form (index_dim 128, Hi <= 64); d_k already zeroed.
+cudaError_t launch_indexer_kl_grad_tc(const IndexerKlArgs &a, cudaStream_t stream);
 // Largest topk (entries of sparse_indices per token) the kernel accepts.
 int32_t indexer_kl_max_topk();
 
