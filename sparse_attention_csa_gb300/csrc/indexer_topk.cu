@@ -23,9 +23,10 @@
 //     sequence (each with its own row range); visibility masks per token.
 //   * Scores of the group stay in shared memory (global scratch when a
 //     sequence offers more than kScoreCap rows); afterwards each of the four
-//     epilogue warps selects one token's top-k with a warp-level 4-pass 8-bit
-//     radix select on order-preserving keys and emits the winners in row
-//     order with warp scans.
+//     epilogue warps selects one token's top-k with a warp-level radix select
+//     on order-preserving keys (8-bit digits below the bits all of the
+//     token's keys share, stopping once the threshold bucket is taken whole)
+//     and emits the winners in row order with warp ballots.
 //   * A token that sees at most topk blocks selects all of them whatever
 //     their scores, so unless the caller asks for the values it is not scored
 //     at all: a first pass marks the CTA's groups that hold a token to score,
@@ -77,7 +78,7 @@ struct Misc {
     uint32_t tmem_base;
     int32_t abort;
     GroupInfo info[2];
-    float w[kG * 64];
+    alignas(16) float w[kG * 64];
     int32_t hist[4][256];
     int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
     uint32_t gscored[kGrpBits / 32];             // this CTA's groups with a token to score
@@ -129,11 +130,48 @@ __device__ __forceinline__ int32_t warp_excl_scan(int32_t v, int lane, int32_t *
     return x - v;
 }
 
+// Scores in shared memory are read with shared-space loads (the score row
+// pointer is generic: it may point to the global spill buffer instead).
+template <bool kShared>
+struct ScoreRow {
+    const float *p;
+    uint32_t s;  // shared-space address of p when kShared
+    __device__ __forceinline__ explicit ScoreRow(const float *ptr)
+        : p(ptr), s(kShared ? (uint32_t)__cvta_generic_to_shared(ptr) : 0u) {}
+    __device__ __forceinline__ float operator[](int32_t i) const {
+        if constexpr (kShared) {
+            float v;
+            asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(s + 4u * (uint32_t)i));
+            return v;
+        } else {
+            return p[i];
+        }
+    }
+};
+
+__device__ __forceinline__ void hist_add(uint32_t hist_s, uint32_t bin) {
+    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hist_s + 4u * bin) : "memory");
+}
+
 // One warp selects the top K of sc[0..n) (ties to the lower index) and writes
 // them in ascending index order as base + index (values alongside).
-__device__ void warp_topk(const float *sc, int32_t n, int32_t K, int32_t base,
+// Radix select on order-preserving keys: a first sweep finds the smallest and
+// largest key, whose common leading bits every key shares (scores of one
+// token often share sign and exponent); the digits below them are then fixed
+// 8 bits a sweep from the top. Each sweep counts, in a 256-bin shared
+// histogram, the keys that match the digits fixed so far, and fixes the next
+// digit as the one holding the K-th largest; the search stops once every key
+// of that bucket is taken (its count equals what is left to take), usually
+// after two or three sweeps. One more sweep emits, 32 consecutive indices at
+// a time, every key above the bucket and the bucket's keys in index order up
+// to the count left (so equal keys go to the lower index). Every sweep loads
+// kBatch scores per lane before using any, so that the loads overlap.
+template <bool kShared>
+__device__ void warp_topk(const float *scores, int32_t n, int32_t K, int32_t base,
                           int32_t *__restrict__ idx_row, float *__restrict__ val_row,
                           int32_t *hist, int lane) {
+    const ScoreRow<kShared> sc(scores);
+    const uint32_t hist_s = (uint32_t)__cvta_generic_to_shared(hist);
     if (n <= K) {
         for (int32_t i = lane; i < K; i += 32) {
             idx_row[i] = i < n ? base + i : -1;
@@ -141,17 +179,45 @@ __device__ void warp_topk(const float *sc, int32_t n, int32_t K, int32_t base,
         }
         return;
     }
-    uint32_t prefix = 0, mask = 0;
+    constexpr int kBatch = 8;
+    uint32_t keys[kBatch];
+    auto load_keys = [&](int32_t i0) {  // indices i0 + 32 m + lane
+        float v[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) v[m] = sc[min(i0 + 32 * m + lane, n - 1)];  // in bounds
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) keys[m] = i0 + 32 * m + lane < n ? float_key(v[m]) : 0u;
+    };
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int32_t i0 = 0; i0 < n; i0 += 32 * kBatch) {
+        load_keys(i0);
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m)
+            if (i0 + 32 * m + lane < n) {
+                lo = min(lo, keys[m]);
+                hi = max(hi, keys[m]);
+            }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    // bits below the common leading ones: 0 when every key is equal
+    const int free_bits = (lo == hi) ? 0 : 32 - __clz((int)(lo ^ hi));
+    uint32_t mask = free_bits == 32 ? 0u : ~((1u << free_bits) - 1u);
+    uint32_t prefix = lo & mask;
     int32_t k_rem = K;
 #pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
+    for (int top = free_bits; top > 0; top -= 8) {
+        const int shift = max(top - 8, 0);
+        const uint32_t dmask = (1u << (top - shift)) - 1u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) hist[lane + 32 * i] = 0;
         __syncwarp();
-        for (int32_t i = lane; i < n; i += 32) {
-            const uint32_t u = float_key(sc[i]);
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+        for (int32_t i0 = 0; i0 < n; i0 += 32 * kBatch) {
+            load_keys(i0);
+#pragma unroll
+            for (int m = 0; m < kBatch; ++m)
+                if (i0 + 32 * m + lane < n && (keys[m] & mask) == prefix)
+                    hist_add(hist_s, (keys[m] >> shift) & dmask);
         }
         __syncwarp();
         int32_t c[8], local = 0;
@@ -162,12 +228,13 @@ __device__ void warp_topk(const float *sc, int32_t n, int32_t K, int32_t base,
         }
         int32_t tot;
         int32_t above = warp_excl_scan(local, lane, &tot);
-        int32_t my_digit = -1, my_above = 0;
+        int32_t my_digit = -1, my_above = 0, my_count = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (above < k_rem && k_rem <= above + c[i]) {
                 my_digit = 255 - (lane * 8 + i);
                 my_above = above;
+                my_count = c[i];
             }
             above += c[i];
         }
@@ -175,35 +242,57 @@ __device__ void warp_topk(const float *sc, int32_t n, int32_t K, int32_t base,
         const int src = who ? __ffs(who) - 1 : 0;
         const int32_t digit = __shfl_sync(0xffffffffu, my_digit, src);
         k_rem -= __shfl_sync(0xffffffffu, my_above, src);
+        const int32_t count = __shfl_sync(0xffffffffu, my_count, src);
         prefix |= (uint32_t)max(digit, 0) << shift;
-        mask |= 255u << shift;
+        mask |= dmask << shift;
         __syncwarp();
+        if (count == k_rem) break;  // the whole bucket is taken
     }
-    const uint32_t tau = prefix;
-    const int32_t per = (n + 31) / 32;
-    const int32_t c0 = min(n, lane * per), c1 = min(n, c0 + per);
-    int32_t gt = 0, eq = 0;
-    for (int32_t i = c0; i < c1; ++i) {
-        const uint32_t u = float_key(sc[i]);
-        gt += u > tau;
-        eq += u == tau;
-    }
-    int32_t tot;
-    const int32_t eq_before = warp_excl_scan(eq, lane, &tot);
-    const int32_t my_eq = max(0, min(eq, k_rem - eq_before));
-    int32_t pos = warp_excl_scan(gt + my_eq, lane, &tot);
-    int32_t seen = 0;
-    for (int32_t i = c0; i < c1; ++i) {
-        const uint32_t u = float_key(sc[i]);
-        bool take = u > tau;
-        if (u == tau) {
-            take = seen < my_eq;
-            ++seen;
+    // Emission: all ballots of a batch first (they do not depend on one
+    // another), then the running counts as warp-uniform integers, then each
+    // lane's stores.
+    const uint32_t below = (1u << lane) - 1u;
+    int32_t pos = 0, eq_seen = 0;
+    for (int32_t i0 = 0; i0 < n; i0 += 32 * kBatch) {
+        load_keys(i0);
+        uint32_t gts[kBatch], eqs[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            const bool in = i0 + 32 * m + lane < n;
+            const uint32_t mu = keys[m] & mask;
+            gts[m] = __ballot_sync(0xffffffffu, in && mu > prefix);
+            eqs[m] = __ballot_sync(0xffffffffu, in && mu == prefix);
         }
-        if (take && pos < K) {  // exactly K are taken; the bound only guards the row
-            idx_row[pos] = base + i;
-            if (val_row) val_row[pos] = sc[i];
-            ++pos;
+        uint32_t takes[kBatch];
+        int32_t before[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            // the bucket's keys of this round that are still taken: the first
+            // `quota` set bits of eqs[m]
+            const int32_t ne = __popc(eqs[m]);
+            const int32_t quota = k_rem - eq_seen;
+            uint32_t eq_take = eqs[m];
+            if (quota <= 0) {
+                eq_take = 0u;
+            } else if (quota < ne) {
+                uint32_t x = eqs[m];  // clear its quota - 1 lowest set bits
+                for (int32_t j = 1; j < quota; ++j) x &= x - 1u;
+                const int last = __ffs(x) - 1;  // the quota-th set bit
+                eq_take &= last >= 31 ? 0xffffffffu : ((2u << last) - 1u);
+            }
+            takes[m] = gts[m] | eq_take;
+            before[m] = pos;
+            pos += __popc(takes[m]);
+            eq_seen += ne;
+        }
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            if ((takes[m] >> lane) & 1u) {
+                const int32_t i = i0 + 32 * m + lane;
+                const int32_t p = before[m] + __popc(takes[m] & below);
+                idx_row[p] = base + i;
+                if (val_row) val_row[p] = sc[min(i, n - 1)];  // i < n: taken
+            }
         }
     }
 }
@@ -578,17 +667,50 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         float acc[kG];
 #pragma unroll
                         for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
+                        if constexpr (HPAD >= 32) {
+                            // 32-column chunks lie inside one token: two chunks per
+                            // tensor-memory wait, weights as float4, two partial
+                            // sums per token
+                            float part[kG][2];
 #pragma unroll
-                        for (int cc = 0; cc < (N + 31) / 32; ++cc) {
-                            float x[32];
-                            tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x);
-                            tc::tmem_wait_ld();
+                            for (int g = 0; g < kG; ++g) part[g][0] = part[g][1] = 0.0f;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int col = 32 * cc + i;
-                                if (col < N) {
-                                    const int g = col / HPAD, h = col % HPAD;
-                                    acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
+                            for (int cc = 0; cc < N / 32; cc += 2) {
+                                float x[2][32];
+                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x[0]);
+                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc + 32, x[1]);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int half = 0; half < 2; ++half) {
+                                    const int c0 = 32 * (cc + half);
+                                    const int g = c0 / HPAD, h0 = c0 % HPAD;
+                                    const float4 *wv = reinterpret_cast<const float4 *>(ms->w + g * 64 + h0);
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) {
+                                        const float4 w4 = wv[i];
+                                        const float *xi = x[half] + 4 * i;
+                                        part[g][0] = fmaf(w4.x, fmaxf(xi[0], 0.0f), part[g][0]);
+                                        part[g][1] = fmaf(w4.y, fmaxf(xi[1], 0.0f), part[g][1]);
+                                        part[g][0] = fmaf(w4.z, fmaxf(xi[2], 0.0f), part[g][0]);
+                                        part[g][1] = fmaf(w4.w, fmaxf(xi[3], 0.0f), part[g][1]);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int g = 0; g < kG; ++g) acc[g] = part[g][0] + part[g][1];
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < (N + 31) / 32; ++cc) {
+                                float x[32];
+                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const int col = 32 * cc + i;
+                                    if (col < N) {
+                                        const int g = col / HPAD, h = col % HPAD;
+                                        acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
+                                    }
                                 }
                             }
                         }
@@ -611,8 +733,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
                     float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
                     const int32_t n = gi.valid ? gi.nv[g] : 0;
-                    warp_topk(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row, val_row,
-                              ms->hist[sel_warp], lane);
+                    if (gi.spill)
+                        warp_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                         val_row, ms->hist[sel_warp], lane);
+                    else
+                        warp_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                        val_row, ms->hist[sel_warp], lane);
                 }
             }
             tc::named_bar_sync(1, 128);  // scores free for the next group
