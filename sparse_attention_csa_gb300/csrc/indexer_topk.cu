@@ -44,12 +44,13 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, MMA, 8 epilogue + selection warps
+constexpr int kEpiThreads = 256;
 constexpr int kG = 4;               // tokens per group
 constexpr int kTileRows = 128;      // compressed rows per MMA tile
 constexpr int kScoreCap = 5120;     // rows per token kept in shared memory
 constexpr int kMaxCtas = 1024;      // persistent grid bound (sizes the scratch)
-constexpr int kCuCap = 500;         // sequences whose offsets are staged in shared memory
+constexpr int kCuCap = 250;         // sequences whose offsets are staged in shared memory
 constexpr int kGrpBits = 4096;      // groups per CTA tracked by the scored-group bitmap
 
 // shared memory map (1024-aligned base)
@@ -79,7 +80,8 @@ struct Misc {
     int32_t abort;
     GroupInfo info[2];
     alignas(16) float w[kG * 64];
-    int32_t hist[4][256];
+    int32_t hist[4][2][256];  // per token: two rounds of packed counts (two warps)
+    uint32_t xch[4][4];       // per token: the two warps' smallest and largest keys
     int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
     uint32_t gscored[kGrpBits / 32];             // this CTA's groups with a token to score
 };
@@ -92,7 +94,7 @@ __device__ __forceinline__ bool bar_red_and(bool v) {
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
         : "r"((uint32_t)v)
@@ -297,6 +299,181 @@ __device__ void warp_topk(const float *scores, int32_t n, int32_t K, int32_t bas
     }
 }
 
+// The same selection by two warps (part 0 and part 1, on the same scheduler,
+// joined by the 64-thread named barrier `bar`), each sweeping one contiguous
+// half of the scores: the smallest and largest keys are exchanged through
+// `xch`, and each pass's histogram holds both halves' counts packed in one
+// word (part 0 in the low 16 bits, part 1 in the high), so that both warps
+// fix the same digit and each also learns how many keys of its own half lie
+// above the bucket and in it. Part 1's first output slot is then part 0's
+// count above the bucket plus the bucket keys part 0 takes, with no further
+// exchange. Two rounds of histograms alternate, so one barrier separates a
+// pass's reads from the next pass's zeroing. Rows of more than kPairMax
+// scores (16-bit counts) go to warp_topk on part 0 alone.
+constexpr int32_t kPairMax = 130000;
+
+template <bool kShared>
+__device__ void pair_topk(const float *scores, int32_t n, int32_t K, int32_t base,
+                          int32_t *__restrict__ idx_row, float *__restrict__ val_row,
+                          int32_t (*hist)[256], uint32_t *xch, int part, int lane, uint32_t bar) {
+    if (n > kPairMax) {
+        if (part == 0) warp_topk<kShared>(scores, n, K, base, idx_row, val_row, hist[0], lane);
+        return;
+    }
+    const ScoreRow<kShared> sc(scores);
+    if (n <= K) {
+        for (int32_t i = lane + 32 * part; i < K; i += 64) {
+            idx_row[i] = i < n ? base + i : -1;
+            if (val_row) val_row[i] = i < n ? sc[i] : -INFINITY;
+        }
+        return;
+    }
+    constexpr int kBatch = 8, kSpan = 32 * kBatch;
+    const int32_t nb = (n + kSpan - 1) / kSpan, nbh = (nb + 1) / 2;
+    const int32_t split = min(n, nbh * kSpan);  // part 0: [0, split), part 1: [split, n)
+    const int32_t r0 = part ? split : 0, r1 = part ? n : split;
+    uint32_t keys[kBatch];
+    auto load_keys = [&](int32_t i0) {  // indices i0 + 32 m + lane of this half
+        float v[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) v[m] = sc[min(i0 + 32 * m + lane, n - 1)];  // in bounds
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) keys[m] = i0 + 32 * m + lane < r1 ? float_key(v[m]) : 0u;
+    };
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int32_t i0 = r0; i0 < r1; i0 += kSpan) {
+        load_keys(i0);
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m)
+            if (i0 + 32 * m + lane < r1) {
+                lo = min(lo, keys[m]);
+                hi = max(hi, keys[m]);
+            }
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+        xch[2 * part] = lo;
+        xch[2 * part + 1] = hi;
+    }
+    tc::named_bar_sync(bar, 64);
+    lo = min(xch[0], xch[2]);
+    hi = max(xch[1], xch[3]);
+    const int free_bits = (lo == hi) ? 0 : 32 - __clz((int)(lo ^ hi));
+    uint32_t mask = free_bits == 32 ? 0u : ~((1u << free_bits) - 1u);
+    uint32_t prefix = lo & mask;
+    int32_t k_rem = K;
+    // keys of each half above the bucket and in it (all of them when every
+    // key is equal and no pass runs)
+    int32_t above0 = 0, above1 = 0, eq0 = split, eq1 = n - split;
+    int hb = 0;
+#pragma unroll 1
+    for (int top = free_bits; top > 0; top -= 8, hb ^= 1) {
+        const int shift = max(top - 8, 0);
+        const uint32_t dmask = (1u << (top - shift)) - 1u;
+        int32_t *H = hist[hb];
+        const uint32_t hs = (uint32_t)__cvta_generic_to_shared(H);
+        for (int i = lane + 32 * part; i < 256; i += 64) H[i] = 0;
+        tc::named_bar_sync(bar, 64);
+        const uint32_t one = part ? 65536u : 1u;
+        for (int32_t i0 = r0; i0 < r1; i0 += kSpan) {
+            load_keys(i0);
+#pragma unroll
+            for (int m = 0; m < kBatch; ++m)
+                if (i0 + 32 * m + lane < r1 && (keys[m] & mask) == prefix)
+                    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(hs + 4u * ((keys[m] >> shift) & dmask)),
+                                 "r"(one)
+                                 : "memory");
+        }
+        tc::named_bar_sync(bar, 64);
+        uint32_t cw[8];
+        int32_t c[8], local = 0, local0 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            cw[i] = (uint32_t)H[255 - (lane * 8 + i)];
+            c[i] = (int32_t)((cw[i] & 0xffffu) + (cw[i] >> 16));
+            local += c[i];
+            local0 += (int32_t)(cw[i] & 0xffffu);
+        }
+        int32_t tot;
+        int32_t above = warp_excl_scan(local, lane, &tot);
+        int32_t a0 = warp_excl_scan(local0, lane, &tot);
+        int32_t my_digit = -1, my_above = 0, my_a0 = 0;
+        uint32_t my_cw = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (above < k_rem && k_rem <= above + c[i]) {
+                my_digit = 255 - (lane * 8 + i);
+                my_above = above;
+                my_a0 = a0;
+                my_cw = cw[i];
+            }
+            above += c[i];
+            a0 += (int32_t)(cw[i] & 0xffffu);
+        }
+        const uint32_t who = __ballot_sync(0xffffffffu, my_digit >= 0);
+        const int src = who ? __ffs(who) - 1 : 0;
+        const int32_t digit = __shfl_sync(0xffffffffu, my_digit, src);
+        const int32_t A = __shfl_sync(0xffffffffu, my_above, src);
+        const int32_t A0 = __shfl_sync(0xffffffffu, my_a0, src);
+        const uint32_t bucket = __shfl_sync(0xffffffffu, my_cw, src);
+        k_rem -= A;
+        above0 += A0;
+        above1 += A - A0;
+        eq0 = (int32_t)(bucket & 0xffffu);
+        eq1 = (int32_t)(bucket >> 16);
+        prefix |= (uint32_t)max(digit, 0) << shift;
+        mask |= dmask << shift;
+        if (eq0 + eq1 == k_rem) break;  // the whole bucket is taken
+    }
+    (void)above1;
+    // emission of this half: part 1 starts after what part 0 takes
+    int32_t pos = part ? above0 + min(eq0, k_rem) : 0;
+    const int32_t quota = part ? max(0, k_rem - eq0) : k_rem;
+    const uint32_t below = (1u << lane) - 1u;
+    int32_t eq_seen = 0;
+    for (int32_t i0 = r0; i0 < r1; i0 += kSpan) {
+        load_keys(i0);
+        uint32_t gts[kBatch], eqs[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            const bool in = i0 + 32 * m + lane < r1;
+            const uint32_t mu = keys[m] & mask;
+            gts[m] = __ballot_sync(0xffffffffu, in && mu > prefix);
+            eqs[m] = __ballot_sync(0xffffffffu, in && mu == prefix);
+        }
+        uint32_t takes[kBatch];
+        int32_t before[kBatch];
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            const int32_t ne = __popc(eqs[m]);
+            const int32_t left = quota - eq_seen;
+            uint32_t eq_take = eqs[m];
+            if (left <= 0) {
+                eq_take = 0u;
+            } else if (left < ne) {
+                uint32_t x = eqs[m];  // clear its left - 1 lowest set bits
+                for (int32_t j = 1; j < left; ++j) x &= x - 1u;
+                const int last = __ffs(x) - 1;  // the left-th set bit
+                eq_take &= last >= 31 ? 0xffffffffu : ((2u << last) - 1u);
+            }
+            takes[m] = gts[m] | eq_take;
+            before[m] = pos;
+            pos += __popc(takes[m]);
+            eq_seen += ne;
+        }
+#pragma unroll
+        for (int m = 0; m < kBatch; ++m) {
+            if ((takes[m] >> lane) & 1u) {
+                const int32_t i = i0 + 32 * m + lane;
+                const int32_t p = before[m] + __popc(takes[m] & below);
+                idx_row[p] = base + i;
+                if (val_row) val_row[p] = sc[min(i, n - 1)];  // i < n: taken
+            }
+        }
+    }
+}
+
 template <int HPAD, int DI>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -320,9 +497,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             tc::mbar_init(&ms->a_full[i], 1);
             tc::mbar_init(&ms->a_empty[i], 1);
             tc::mbar_init(&ms->acc_full[i], 1);
-            tc::mbar_init(&ms->acc_empty[i], 128);
+            tc::mbar_init(&ms->acc_empty[i], kEpiThreads);
             tc::mbar_init(&ms->info_full[i], 1);
-            tc::mbar_init(&ms->info_empty[i], 5);
+            tc::mbar_init(&ms->info_empty[i], 9);  // the MMA thread and 8 epilogue warps
         }
         tc::mbar_init(&ms->drain, 1);
         ms->abort = 0;
@@ -583,10 +760,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         __syncwarp();
     } else {
         // =========================================== epilogue + selection
+        // Warps 2..9: TMEM lane quarter q4 (the warp's own), column half `half`
+        // (tokens 2 half and 2 half + 1 of the group); in the selection, warps
+        // 2 + g and 6 + g (the same scheduler) select token g together.
         const int q4 = warp & 3;
         const int row = 32 * q4 + lane;
         const int ltid = tid - 64;
-        const int sel_warp = warp - 2;  // token of the group this warp selects for
+        const int half = (warp - 2) >> 2;
+        const int sel_tok = (warp - 2) & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
         // Rows of the groups with nothing to score, written first (while the
@@ -595,7 +776,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // when aligned).
         if (bulk) {
             const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
-            for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += 128) {
+            for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += kEpiThreads) {
                 const int64_t li = base + lane;
                 const int64_t k = li / kG;
                 int32_t t = -1, n = 0, cb = 0;
@@ -646,12 +827,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 sc_stride = kScoreCap;
             }
             // weights of the group's tokens (0 beyond Hi / T), if any is scored
-            for (int i = ltid; gi.n_pass > 0 && i < kG * 64; i += 128) {
+            for (int i = ltid; gi.n_pass > 0 && i < kG * 64; i += kEpiThreads) {
                 const int g = i >> 6, h = i & 63;
                 const int32_t t = gi.t0 + g;
                 ms->w[i] = (h < a.Hi && t < a.T) ? __ldg(a.w + (int64_t)t * a.Hi + h) : 0.0f;
             }
-            tc::named_bar_sync(1, 128);
+            tc::named_bar_sync(1, kEpiThreads);
             bool stop = false;
             if (gi.valid) {
                 for (int p = 0; p < gi.n_pass && !stop; ++p) {
@@ -668,27 +849,29 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                         for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
                         if constexpr (HPAD >= 32) {
-                            // 32-column chunks lie inside one token: two chunks per
-                            // tensor-memory wait, weights as float4, two partial
-                            // sums per token
+                            // 32-column chunks lie inside one token: this warp's
+                            // half of the columns, two chunks per tensor-memory
+                            // wait, weights as float4, two partial sums per token
                             float part[kG][2];
 #pragma unroll
                             for (int g = 0; g < kG; ++g) part[g][0] = part[g][1] = 0.0f;
+                            constexpr int kHalfChunks = N / 64;  // 32-column chunks per half
 #pragma unroll
-                            for (int cc = 0; cc < N / 32; cc += 2) {
+                            for (int k = 0; k < kHalfChunks; k += 2) {
+                                const int cc = half * kHalfChunks + k;
                                 float x[2][32];
                                 tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x[0]);
                                 tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc + 32, x[1]);
                                 tc::tmem_wait_ld();
 #pragma unroll
-                                for (int half = 0; half < 2; ++half) {
-                                    const int c0 = 32 * (cc + half);
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    const int c0 = 32 * (cc + hh);
                                     const int g = c0 / HPAD, h0 = c0 % HPAD;
                                     const float4 *wv = reinterpret_cast<const float4 *>(ms->w + g * 64 + h0);
 #pragma unroll
                                     for (int i = 0; i < 8; ++i) {
                                         const float4 w4 = wv[i];
-                                        const float *xi = x[half] + 4 * i;
+                                        const float *xi = x[hh] + 4 * i;
                                         part[g][0] = fmaf(w4.x, fmaxf(xi[0], 0.0f), part[g][0]);
                                         part[g][1] = fmaf(w4.y, fmaxf(xi[1], 0.0f), part[g][1]);
                                         part[g][0] = fmaf(w4.z, fmaxf(xi[2], 0.0f), part[g][0]);
@@ -699,6 +882,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                             for (int g = 0; g < kG; ++g) acc[g] = part[g][0] + part[g][1];
                         } else {
+                            // fewer than 32 heads: all N (<= 128) columns from
+                            // column 0; this warp keeps its half's tokens
 #pragma unroll
                             for (int cc = 0; cc < (N + 31) / 32; ++cc) {
                                 float x[32];
@@ -707,7 +892,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) {
                                     const int col = 32 * cc + i;
-                                    if (col < N) {
+                                    if (col < N && (col / HPAD) >> 1 == half) {
                                         const int g = col / HPAD, h = col % HPAD;
                                         acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
                                     }
@@ -719,29 +904,29 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         const int32_t jl = j * kTileRows + row;
 #pragma unroll
                         for (int g = 0; g < kG; ++g)
-                            if (((ps.mask >> g) & 1) && jl < gi.nv[g])
+                            if ((g >> 1) == half && ((ps.mask >> g) & 1) && jl < gi.nv[g])
                                 sc[(int64_t)g * sc_stride + jl] = acc[g];
                     }
                 }
             }
             if (stop) break;
-            tc::named_bar_sync(1, 128);  // scores complete
+            tc::named_bar_sync(1, kEpiThreads);  // scores complete
             {
-                const int g = sel_warp;
+                const int g = sel_tok;
                 const int32_t t = gi.t0 + g;
                 if (t < a.T) {
                     int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
                     float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
                     const int32_t n = gi.valid ? gi.nv[g] : 0;
                     if (gi.spill)
-                        warp_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                         val_row, ms->hist[sel_warp], lane);
+                        pair_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                         val_row, ms->hist[g], ms->xch[g], half, lane, 2 + g);
                     else
-                        warp_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                        val_row, ms->hist[sel_warp], lane);
+                        pair_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                        val_row, ms->hist[g], ms->xch[g], half, lane, 2 + g);
                 }
             }
-            tc::named_bar_sync(1, 128);  // scores free for the next group
+            tc::named_bar_sync(1, kEpiThreads);  // scores free for the next group
             if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
         }
     }
