@@ -22,19 +22,20 @@
 //   * A group whose tokens span several sequences is processed as one pass per
 //     sequence (each with its own row range); visibility masks per token.
 //   * Scores of the group stay in shared memory (global scratch when a
-//     sequence offers more than kScoreCap rows); afterwards each of the four
-//     epilogue warps selects one token's top-k with a warp-level radix select
-//     on order-preserving keys (8-bit digits below the bits all of the
-//     token's keys share, stopping once the threshold bucket is taken whole)
-//     and emits the winners in row order with warp ballots.
+//     sequence offers more than kScoreCap rows); afterwards each token's
+//     top-k is selected by two epilogue warps of one scheduler (pair_topk):
+//     a radix select on order-preserving keys with 8-bit digits below the
+//     bits all of the token's keys share, stopping once the threshold bucket
+//     is taken whole, and an emission in row order.
 //   * A token that sees at most topk blocks selects all of them whatever
 //     their scores, so unless the caller asks for the values it is not scored
 //     at all: a first pass marks the CTA's groups that hold a token to score,
-//     only those go through the pipeline, and the four epilogue warps write
+//     only those go through the pipeline, and the eight epilogue warps write
 //     every other row (16-byte stores) while the pipeline's loads and first
 //     MMAs run.
-//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
-//     and selection. Every mbarrier wait is bounded.
+//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-9 epilogue
+//     (TMEM lane quarter x column half) and selection. Every mbarrier wait is
+//     bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
