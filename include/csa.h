@@ -390,8 +390,8 @@ csa_status_t csa_indexer_topk_bsnd(const csa_bf16_t *q, const csa_bf16_t *k, con
  * that array until the process exits. The call allocates nothing.
  *
  * Limits and sharing:
- *   - total_cmp above 2,097,152 rows (one CTA's slot, the scores of four
- *     tokens, no longer fits in the array) -> CSA_ERR_WORKSPACE; other
+ *   - total_cmp above 2,097,152 rows (one CTA's slot, two buffers of two
+ *     tokens' scores, no longer fits in the array) -> CSA_ERR_WORKSPACE; other
  *     errors as csa_indexer_topk.
  *   - When scores may spill, the grid is limited to as many CTAs as the
  *     array has slots of 4 x total_cmp floats.

@@ -12,29 +12,32 @@
 // -1 / -inf padding.
 //
 // Design (persistent grid, 1 CTA per SM):
-//   * Four consecutive tokens form a group. The contraction is done with the
+//   * Two consecutive tokens form a group. The contraction is done with the
 //     compressed rows on the MMA's M side and the group's (token, head) pairs
 //     on N:   S^T[j, (g,h)] = k[j, :] . q[t0+g, h, :]
-//     (M = 128 rows, N = 4 x Hpad <= 256, K = Di), accumulated in fp32 in
-//     tensor memory, double-buffered (2 x 256 columns) so the epilogue of one
-//     tile overlaps the MMA of the next. With one TMEM lane per row j, the head
-//     reduction sum_h w*relu(.) runs inside each thread.
+//     (M = 128 rows, N = 2 x Hpad <= 128, K = Di), accumulated in fp32 in
+//     tensor memory, four accumulators of 128 columns, so the epilogue of one
+//     tile overlaps the MMAs of the next ones; k tiles come in three stages.
+//     With one TMEM lane per row j, the head reduction sum_h w*relu(.) runs
+//     inside each thread.
 //   * A group whose tokens span several sequences is processed as one pass per
 //     sequence (each with its own row range); visibility masks per token.
-//   * Scores of the group stay in shared memory (global scratch when a
-//     sequence offers more than kScoreCap rows); afterwards each token's
-//     top-k is selected by two epilogue warps of one scheduler (pair_topk):
-//     a radix select on order-preserving keys with 8-bit digits below the
-//     bits all of the token's keys share, stopping once the threshold bucket
-//     is taken whole, and an emission in row order.
+//   * The scores of a group go to one of two buffers in shared memory (global
+//     scratch when a sequence offers more than kScoreCap rows). Four
+//     selection warps select the top-k of one group while the four epilogue
+//     warps score the next into the other buffer: each token's selection is
+//     done by two warps (pair_topk), a radix select on order-preserving keys
+//     with 8-bit digits below the bits all of the token's keys share,
+//     stopping once the threshold bucket is taken whole, and an emission in
+//     row order.
 //   * A token that sees at most topk blocks selects all of them whatever
 //     their scores, so unless the caller asks for the values it is not scored
 //     at all: a first pass marks the CTA's groups that hold a token to score,
-//     only those go through the pipeline, and the eight epilogue warps write
-//     every other row (16-byte stores) while the pipeline's loads and first
-//     MMAs run.
-//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-9 epilogue
-//     (TMEM lane quarter x column half) and selection. Every mbarrier wait is
+//     only those go through the pipeline, and the epilogue warps write every
+//     other row (16-byte stores) while the pipeline's loads and first MMAs
+//     run.
+//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
+//     (one TMEM lane quarter each), 6-9 selection. Every mbarrier wait is
 //     bounded.
 #include "common.cuh"
 #include "internal.h"
@@ -45,9 +48,13 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 320;   // producer, MMA, 8 epilogue + selection warps
-constexpr int kEpiThreads = 256;
-constexpr int kG = 4;               // tokens per group
+constexpr int kThreads = 320;   // producer, MMA, 4 epilogue warps, 4 selection warps
+constexpr int kEpiThreads = 128;
+constexpr int kSelThreads = 128;
+constexpr int kG = 2;               // tokens per group
+constexpr int kStagesA = 3;         // k tile stages
+constexpr int kAccBufs = 4;         // tensor-memory accumulators (128 columns each)
+constexpr int kInfoSlots = 4;       // group descriptors in flight
 constexpr int kTileRows = 128;      // compressed rows per MMA tile
 constexpr int kScoreCap = 5120;     // rows per token kept in shared memory
 constexpr int kMaxCtas = 1024;      // persistent grid bound (sizes the scratch)
@@ -55,10 +62,10 @@ constexpr int kCuCap = 250;         // sequences whose offsets are staged in sha
 constexpr int kGrpBits = 4096;      // groups per CTA tracked by the scored-group bitmap
 
 // shared memory map (1024-aligned base)
-constexpr uint32_t kOffB = 0;                 // q group: 2 chunks x [256 rows x 128 B]
-constexpr uint32_t kOffA = 65536;             // k tiles: 2 stages x 2 chunks x 16 KB
-constexpr uint32_t kOffScore = 131072;        // kG x kScoreCap fp32
-constexpr uint32_t kOffMisc = kOffScore + kG * kScoreCap * 4;
+constexpr uint32_t kOffB = 0;                 // q group: 2 chunks x [128 rows x 128 B]
+constexpr uint32_t kOffA = 32768;             // k tiles: kStagesA stages x 2 chunks x 16 KB
+constexpr uint32_t kOffScore = kOffA + kStagesA * 32768;  // 2 buffers x kG x kScoreCap fp32
+constexpr uint32_t kOffMisc = kOffScore + 2 * kG * kScoreCap * 4;
 
 struct Pass {
     int32_t mask, cbase, n_tiles, pad;
@@ -73,16 +80,17 @@ struct GroupInfo {
 
 struct Misc {
     uint64_t b_full, b_empty;
-    uint64_t a_full[2], a_empty[2];
-    uint64_t acc_full[2], acc_empty[2];
-    uint64_t info_full[2], info_empty[2];
+    uint64_t a_full[kStagesA], a_empty[kStagesA];
+    uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+    uint64_t info_full[kInfoSlots], info_empty[kInfoSlots];
+    uint64_t sc_full[2], sc_empty[2];  // score buffers: epilogue -> selection -> epilogue
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
-    GroupInfo info[2];
+    GroupInfo info[kInfoSlots];
     alignas(16) float w[kG * 64];
-    int32_t hist[4][2][256];  // per token: two rounds of packed counts (two warps)
-    uint32_t xch[4][4];       // per token: the two warps' smallest and largest keys
+    int32_t hist[kG][2][256];  // per token: two rounds of packed counts (two warps)
+    uint32_t xch[kG][4];       // per token: the two warps' smallest and largest keys
     int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
     uint32_t gscored[kGrpBits / 32];             // this CTA's groups with a token to score
 };
@@ -90,15 +98,16 @@ struct Misc {
 constexpr size_t kSmemBytes = kOffMisc + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ bool bar_red_and(bool v) {
+// AND of v over the `n` threads of named barrier `id` (whole warps).
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool v) {
     uint32_t out;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 256, p;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(out)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
     return out != 0;
 }
@@ -494,13 +503,21 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     if (tid == 0) {
         tc::mbar_init(&ms->b_full, 1);
         tc::mbar_init(&ms->b_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStagesA; ++i) {
             tc::mbar_init(&ms->a_full[i], 1);
             tc::mbar_init(&ms->a_empty[i], 1);
+        }
+        for (int i = 0; i < kAccBufs; ++i) {
             tc::mbar_init(&ms->acc_full[i], 1);
             tc::mbar_init(&ms->acc_empty[i], kEpiThreads);
+        }
+        for (int i = 0; i < kInfoSlots; ++i) {
             tc::mbar_init(&ms->info_full[i], 1);
-            tc::mbar_init(&ms->info_empty[i], 9);  // the MMA thread and 8 epilogue warps
+            tc::mbar_init(&ms->info_empty[i], 9);  // the MMA thread, 4 epilogue and 4 selection warps
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&ms->sc_full[i], 1);
+            tc::mbar_init(&ms->sc_empty[i], 1);
         }
         tc::mbar_init(&ms->drain, 1);
         ms->abort = 0;
@@ -559,6 +576,47 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
+
+    // Rows of the groups with nothing to score, written by the eight epilogue
+    // and selection warps first (while the producer and the MMA warp start on
+    // the scored groups): 32 tokens found at a time per warp, one row per warp
+    // store round (16-byte stores when aligned).
+    auto bulk_fill = [&]() {
+        if (!bulk) return;
+        const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
+        for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += 256) {
+            const int64_t li = base + lane;
+            const int64_t k = li / kG;
+            int32_t t = -1, n = 0, cb = 0;
+            bool write = false;
+            if (li < my_groups * kG && !((ms->gscored[k >> 5] >> (k & 31)) & 1u)) {
+                t = (int32_t)(((int64_t)blockIdx.x + k * gridDim.x) * kG + li % kG);
+                if (t < a.T) {
+                    write = true;
+                    n = visible(t, &cb);
+                    if (n < 0) {
+                        report_error(a.err, kErrCheck, kKerIndexer, n == -1 ? 1 : 2);
+                        n = 0;
+                    }
+                }
+            }
+            for (uint32_t m = __ballot_sync(0xffffffffu, write); m; m &= m - 1) {
+                const int src = __ffs(m) - 1;
+                const int32_t tw = __shfl_sync(0xffffffffu, t, src);
+                const int32_t nw = __shfl_sync(0xffffffffu, n, src);
+                const int32_t cw = __shfl_sync(0xffffffffu, cb, src);
+                int32_t *idx_row = a.topk_idx + (int64_t)tw * a.topk;
+                if (vec) {
+                    for (int32_t i = 4 * lane; i < a.topk; i += 128)
+                        *reinterpret_cast<int4 *>(idx_row + i) =
+                            make_int4(i < nw ? cw + i : -1, i + 1 < nw ? cw + i + 1 : -1,
+                                      i + 2 < nw ? cw + i + 2 : -1, i + 3 < nw ? cw + i + 3 : -1);
+                } else {
+                    for (int32_t i = lane; i < a.topk; i += 32) idx_row[i] = i < nw ? cw + i : -1;
+                }
+            }
+        }
+    };
 
     if (warp == 0) {
         // ===================================================== producer warp
@@ -658,8 +716,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 continue;
             }
-            const uint32_t slot = it & 1;
-            bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 10);
+            const uint32_t slot = it % kInfoSlots;
+            bool ok = cx.wait(&ms->info_empty[slot], ((it / kInfoSlots) & 1) ^ 1, 10);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (lane == 0) {
                 ms->info[slot] = gi;
@@ -679,8 +737,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             bool broke = false;
             for (int p = 0; p < gi.n_pass && !broke; ++p) {
                 for (int32_t j = 0; j < gi.pass[p].n_tiles; ++j, ++a_n) {
-                    const uint32_t st = a_n & 1;
-                    ok = cx.wait(&ms->a_empty[st], ((a_n >> 1) & 1) ^ 1, 12);
+                    const uint32_t st = a_n % kStagesA;
+                    ok = cx.wait(&ms->a_empty[st], ((a_n / kStagesA) & 1) ^ 1, 12);
                     if (!__all_sync(0xffffffffu, ok)) {
                         broke = true;
                         break;
@@ -688,7 +746,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     if (lane == 0) {
                         tc::mbar_expect_tx(&ms->a_full[st], NCH * 16384u);
                         for (int c = 0; c < NCH; ++c)
-                            tc::tma_load_2d(smem + kOffA + st * 32768 + c * 16384, &k_map,
+                            tc::tma_load_2d(smem + kOffA + st * 32768u + c * 16384, &k_map,
                                             &ms->a_full[st], 64 * c,
                                             gi.pass[p].cbase + j * kTileRows);
                     }
@@ -698,8 +756,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         // end of the stream: a group with valid = -1 stops the other roles
         if (!quit) {
-            const uint32_t slot = it & 1;
-            const bool ok = cx.wait(&ms->info_empty[slot], ((it >> 1) & 1) ^ 1, 15);
+            const uint32_t slot = it % kInfoSlots;
+            const bool ok = cx.wait(&ms->info_empty[slot], ((it / kInfoSlots) & 1) ^ 1, 15);
             if (__all_sync(0xffffffffu, ok) && lane == 0) {
                 ms->info[slot].valid = -1;
                 tc::mbar_arrive(&ms->info_full[slot]);
@@ -708,8 +766,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         // drain: every copy issued has landed before the CTA exits
         if (lane == 0) {
             if (b_n > 0 && !tc::mbar_wait(&ms->b_full, (b_n - 1) & 1)) cx.fail(13);
-            for (uint32_t k = (a_n > 2 ? a_n - 2 : 0); k < a_n; ++k)
-                if (!tc::mbar_wait(&ms->a_full[k & 1], (k >> 1) & 1)) cx.fail(14);
+            for (uint32_t k = (a_n > kStagesA ? a_n - kStagesA : 0); k < a_n; ++k)
+                if (!tc::mbar_wait(&ms->a_full[k % kStagesA], (k / kStagesA) & 1)) cx.fail(14);
         }
     } else if (warp == 1) {
         // ========================================================= MMA warp
@@ -720,8 +778,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             uint32_t it = 0, b_n = 0, a_n = 0, t_n = 0;
             bool issued = false;
             for (;; ++it) {
-                const uint32_t slot = it & 1;
-                if (!cx.wait(&ms->info_full[slot], (it >> 1) & 1, 20)) break;
+                const uint32_t slot = it % kInfoSlots;
+                if (!cx.wait(&ms->info_full[slot], (it / kInfoSlots) & 1, 20)) break;
                 const GroupInfo gi = ms->info[slot];
                 tc::mbar_arrive(&ms->info_empty[slot]);
                 if (gi.valid < 0) break;
@@ -731,9 +789,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 bool stop = false;
                 for (int p = 0; p < gi.n_pass && !stop; ++p) {
                     for (int32_t j = 0; j < gi.pass[p].n_tiles; ++j, ++a_n, ++t_n) {
-                        const uint32_t st = a_n & 1, buf = t_n & 1;
-                        if (!cx.wait(&ms->acc_empty[buf], ((t_n >> 1) & 1) ^ 1, 22) ||
-                            !cx.wait(&ms->a_full[st], (a_n >> 1) & 1, 23)) {
+                        const uint32_t st = a_n % kStagesA, buf = t_n % kAccBufs;
+                        if (!cx.wait(&ms->acc_empty[buf], ((t_n / kAccBufs) & 1) ^ 1, 22) ||
+                            !cx.wait(&ms->a_full[st], (a_n / kStagesA) & 1, 23)) {
                             stop = true;
                             break;
                         }
@@ -741,7 +799,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                         for (int kk = 0; kk < DI / 16; ++kk) {
                             const int c = kk / 4, ks = kk % 4;
-                            tc::mma_bf16(tmem + buf * 256,
+                            tc::mma_bf16(tmem + buf * 128,
                                          tc::desc_add(da, st * 32768 + c * 16384 + ks * 32),
                                          tc::desc_add(db, c * kBChunk + ks * 32), idesc, kk > 0);
                         }
@@ -759,175 +817,170 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             }
         }
         __syncwarp();
-    } else {
-        // =========================================== epilogue + selection
-        // Warps 2..9: TMEM lane quarter q4 (the warp's own), column half `half`
-        // (tokens 2 half and 2 half + 1 of the group); in the selection, warps
-        // 2 + g and 6 + g (the same scheduler) select token g together.
+    } else if (warp < 6) {
+        // ================================================== epilogue warps
+        // Warp 2..5: TMEM lane quarter q4 (the warp's own), all N columns.
         const int q4 = warp & 3;
         const int row = 32 * q4 + lane;
         const int ltid = tid - 64;
-        const int half = (warp - 2) >> 2;
-        const int sel_tok = (warp - 2) & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
-        // Rows of the groups with nothing to score, written first (while the
-        // producer and the MMA warp start on the scored groups): 32 tokens found
-        // at a time per warp, one row per warp store round (16-byte stores
-        // when aligned).
-        if (bulk) {
-            const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
-            for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += kEpiThreads) {
-                const int64_t li = base + lane;
-                const int64_t k = li / kG;
-                int32_t t = -1, n = 0, cb = 0;
-                bool write = false;
-                if (li < my_groups * kG && !((ms->gscored[k >> 5] >> (k & 31)) & 1u)) {
-                    t = (int32_t)(((int64_t)blockIdx.x + k * gridDim.x) * kG + li % kG);
-                    if (t < a.T) {
-                        write = true;
-                        n = visible(t, &cb);
-                        if (n < 0) {
-                            report_error(a.err, kErrCheck, kKerIndexer, n == -1 ? 1 : 2);
-                            n = 0;
-                        }
-                    }
-                }
-                for (uint32_t m = __ballot_sync(0xffffffffu, write); m; m &= m - 1) {
-                    const int src = __ffs(m) - 1;
-                    const int32_t tw = __shfl_sync(0xffffffffu, t, src);
-                    const int32_t nw = __shfl_sync(0xffffffffu, n, src);
-                    const int32_t cw = __shfl_sync(0xffffffffu, cb, src);
-                    int32_t *idx_row = a.topk_idx + (int64_t)tw * a.topk;
-                    if (vec) {
-                        for (int32_t i = 4 * lane; i < a.topk; i += 128)
-                            *reinterpret_cast<int4 *>(idx_row + i) =
-                                make_int4(i < nw ? cw + i : -1, i + 1 < nw ? cw + i + 1 : -1,
-                                          i + 2 < nw ? cw + i + 2 : -1, i + 3 < nw ? cw + i + 3 : -1);
-                    } else {
-                        for (int32_t i = lane; i < a.topk; i += 32) idx_row[i] = i < nw ? cw + i : -1;
-                    }
-                }
-            }
-        }
-        uint32_t it = 0, t_n = 0;
+        bulk_fill();
+        uint32_t it = 0, t_n = 0, sc_n = 0;
         for (;; ++it) {
-            const uint32_t slot = it & 1;
-            bool ok = cx.wait(&ms->info_full[slot], (it >> 1) & 1, 30);
-            if (!bar_red_and(ok)) break;
+            const uint32_t slot = it % kInfoSlots;
+            bool ok = cx.wait(&ms->info_full[slot], (it / kInfoSlots) & 1, 30);
+            if (!bar_red_and(1, kEpiThreads, ok)) break;
             // read in place; the slot is released at the end of the group
             const GroupInfo &gi = ms->info[slot];
             if (gi.valid < 0) break;
+            // the score buffer this group fills, once the selection is done
+            // with the group that used it two groups ago
+            const uint32_t b = sc_n & 1;
+            ok = cx.wait(&ms->sc_empty[b], ((sc_n >> 1) & 1) ^ 1, 33);
+            if (!bar_red_and(1, kEpiThreads, ok)) break;
             float *sc;
             int32_t sc_stride;
             if (gi.spill) {
-                sc = a.scratch + (int64_t)blockIdx.x * kG * a.Tc;
+                sc = a.scratch + ((int64_t)blockIdx.x * 2 + b) * kG * a.Tc;
                 sc_stride = a.Tc;
             } else {
-                sc = sc_smem;
+                sc = sc_smem + b * kG * kScoreCap;
                 sc_stride = kScoreCap;
             }
-            // weights of the group's tokens (0 beyond Hi / T), if any is scored
-            for (int i = ltid; gi.n_pass > 0 && i < kG * 64; i += kEpiThreads) {
+            // weights of the group's tokens (0 beyond Hi / T)
+            for (int i = ltid; i < kG * 64; i += kEpiThreads) {
                 const int g = i >> 6, h = i & 63;
                 const int32_t t = gi.t0 + g;
                 ms->w[i] = (h < a.Hi && t < a.T) ? __ldg(a.w + (int64_t)t * a.Hi + h) : 0.0f;
             }
             tc::named_bar_sync(1, kEpiThreads);
             bool stop = false;
-            if (gi.valid) {
-                for (int p = 0; p < gi.n_pass && !stop; ++p) {
-                    const Pass &ps = gi.pass[p];
-                    for (int32_t j = 0; j < ps.n_tiles; ++j, ++t_n) {
-                        const uint32_t buf = t_n & 1;
-                        ok = cx.wait(&ms->acc_full[buf], (t_n >> 1) & 1, 31);
-                        if (!bar_red_and(ok)) {
-                            stop = true;
-                            break;
-                        }
-                        tc::tc_fence_after();
-                        float acc[kG];
-#pragma unroll
-                        for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
-                        if constexpr (HPAD >= 32) {
-                            // 32-column chunks lie inside one token: this warp's
-                            // half of the columns, two chunks per tensor-memory
-                            // wait, weights as float4, two partial sums per token
-                            float part[kG][2];
-#pragma unroll
-                            for (int g = 0; g < kG; ++g) part[g][0] = part[g][1] = 0.0f;
-                            constexpr int kHalfChunks = N / 64;  // 32-column chunks per half
-#pragma unroll
-                            for (int k = 0; k < kHalfChunks; k += 2) {
-                                const int cc = half * kHalfChunks + k;
-                                float x[2][32];
-                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x[0]);
-                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc + 32, x[1]);
-                                tc::tmem_wait_ld();
-#pragma unroll
-                                for (int hh = 0; hh < 2; ++hh) {
-                                    const int c0 = 32 * (cc + hh);
-                                    const int g = c0 / HPAD, h0 = c0 % HPAD;
-                                    const float4 *wv = reinterpret_cast<const float4 *>(ms->w + g * 64 + h0);
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        const float4 w4 = wv[i];
-                                        const float *xi = x[hh] + 4 * i;
-                                        part[g][0] = fmaf(w4.x, fmaxf(xi[0], 0.0f), part[g][0]);
-                                        part[g][1] = fmaf(w4.y, fmaxf(xi[1], 0.0f), part[g][1]);
-                                        part[g][0] = fmaf(w4.z, fmaxf(xi[2], 0.0f), part[g][0]);
-                                        part[g][1] = fmaf(w4.w, fmaxf(xi[3], 0.0f), part[g][1]);
-                                    }
-                                }
-                            }
-#pragma unroll
-                            for (int g = 0; g < kG; ++g) acc[g] = part[g][0] + part[g][1];
-                        } else {
-                            // fewer than 32 heads: all N (<= 128) columns from
-                            // column 0; this warp keeps its half's tokens
-#pragma unroll
-                            for (int cc = 0; cc < (N + 31) / 32; ++cc) {
-                                float x[32];
-                                tc::tmem_ld32(lane_addr + buf * 256 + 32 * cc, x);
-                                tc::tmem_wait_ld();
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    const int col = 32 * cc + i;
-                                    if (col < N && (col / HPAD) >> 1 == half) {
-                                        const int g = col / HPAD, h = col % HPAD;
-                                        acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
-                                    }
-                                }
-                            }
-                        }
-                        tc::tc_fence_before();
-                        tc::mbar_arrive(&ms->acc_empty[buf]);
-                        const int32_t jl = j * kTileRows + row;
-#pragma unroll
-                        for (int g = 0; g < kG; ++g)
-                            if ((g >> 1) == half && ((ps.mask >> g) & 1) && jl < gi.nv[g])
-                                sc[(int64_t)g * sc_stride + jl] = acc[g];
+            for (int p = 0; p < gi.n_pass && !stop; ++p) {
+                const Pass &ps = gi.pass[p];
+                for (int32_t j = 0; j < ps.n_tiles; ++j, ++t_n) {
+                    const uint32_t buf = t_n % kAccBufs;
+                    ok = cx.wait(&ms->acc_full[buf], (t_n / kAccBufs) & 1, 31);
+                    if (!bar_red_and(1, kEpiThreads, ok)) {
+                        stop = true;
+                        break;
                     }
+                    tc::tc_fence_after();
+                    const uint32_t col0 = lane_addr + buf * 128;
+                    float acc[kG];
+#pragma unroll
+                    for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
+                    if constexpr (HPAD >= 32) {
+                        // 32-column chunks lie inside one token: two chunks per
+                        // tensor-memory wait, weights as float4, two partial
+                        // sums per token
+                        float part[kG][2];
+#pragma unroll
+                        for (int g = 0; g < kG; ++g) part[g][0] = part[g][1] = 0.0f;
+#pragma unroll
+                        for (int cc = 0; cc < N / 32; cc += 2) {
+                            float x[2][32];
+                            tc::tmem_ld32(col0 + 32 * cc, x[0]);
+                            tc::tmem_ld32(col0 + 32 * cc + 32, x[1]);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int c0 = 32 * (cc + hh);
+                                const int g = c0 / HPAD, h0 = c0 % HPAD;
+                                const float4 *wv = reinterpret_cast<const float4 *>(ms->w + g * 64 + h0);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float4 w4 = wv[i];
+                                    const float *xi = x[hh] + 4 * i;
+                                    part[g][0] = fmaf(w4.x, fmaxf(xi[0], 0.0f), part[g][0]);
+                                    part[g][1] = fmaf(w4.y, fmaxf(xi[1], 0.0f), part[g][1]);
+                                    part[g][0] = fmaf(w4.z, fmaxf(xi[2], 0.0f), part[g][0]);
+                                    part[g][1] = fmaf(w4.w, fmaxf(xi[3], 0.0f), part[g][1]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int g = 0; g < kG; ++g) acc[g] = part[g][0] + part[g][1];
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < (N + 31) / 32; ++cc) {
+                            float x[32];
+                            tc::tmem_ld32(col0 + 32 * cc, x);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int col = 32 * cc + i;
+                                if (col < N) {
+                                    const int g = col / HPAD, h = col % HPAD;
+                                    acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
+                                }
+                            }
+                        }
+                    }
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&ms->acc_empty[buf]);
+                    const int32_t jl = j * kTileRows + row;
+#pragma unroll
+                    for (int g = 0; g < kG; ++g)
+                        if (((ps.mask >> g) & 1) && jl < gi.nv[g])
+                            sc[(int64_t)g * sc_stride + jl] = acc[g];
                 }
             }
             if (stop) break;
-            tc::named_bar_sync(1, kEpiThreads);  // scores complete
-            {
-                const int g = sel_tok;
-                const int32_t t = gi.t0 + g;
-                if (t < a.T) {
-                    int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
-                    float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
-                    const int32_t n = gi.valid ? gi.nv[g] : 0;
-                    if (gi.spill)
-                        pair_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                         val_row, ms->hist[g], ms->xch[g], half, lane, 2 + g);
-                    else
-                        pair_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                        val_row, ms->hist[g], ms->xch[g], half, lane, 2 + g);
-                }
+            // scores complete: hand the buffer to the selection warps (the
+            // barrier orders every epilogue thread's writes before the arrive)
+            __threadfence_block();
+            tc::named_bar_sync(1, kEpiThreads);
+            if (ltid == 0) tc::mbar_arrive(&ms->sc_full[b]);
+            ++sc_n;
+            if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
+        }
+    } else {
+        // ================================================= selection warps
+        // Warps 6, 7 select token 0 of each group and 8, 9 token 1, one half
+        // of the scores each (pair_topk), while the epilogue scores the next
+        // group into the other buffer.
+        const int sel_tok = (warp - 6) >> 1;
+        const int part = (warp - 6) & 1;
+        const int stid = tid - 192;
+        float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
+        bulk_fill();
+        uint32_t it = 0, sc_n = 0;
+        for (;; ++it) {
+            const uint32_t slot = it % kInfoSlots;
+            bool ok = cx.wait(&ms->info_full[slot], (it / kInfoSlots) & 1, 34);
+            if (!bar_red_and(7, kSelThreads, ok)) break;
+            const GroupInfo &gi = ms->info[slot];
+            if (gi.valid < 0) break;
+            const uint32_t b = sc_n & 1;
+            ok = cx.wait(&ms->sc_full[b], (sc_n >> 1) & 1, 35);
+            if (!bar_red_and(7, kSelThreads, ok)) break;
+            const float *sc;
+            int32_t sc_stride;
+            if (gi.spill) {
+                sc = a.scratch + ((int64_t)blockIdx.x * 2 + b) * kG * a.Tc;
+                sc_stride = a.Tc;
+            } else {
+                sc = sc_smem + b * kG * kScoreCap;
+                sc_stride = kScoreCap;
             }
-            tc::named_bar_sync(1, kEpiThreads);  // scores free for the next group
+            const int g = sel_tok;
+            const int32_t t = gi.t0 + g;
+            if (t < a.T) {
+                int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
+                float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
+                const int32_t n = gi.valid ? gi.nv[g] : 0;
+                if (gi.spill)
+                    pair_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                     val_row, ms->hist[g], ms->xch[g], part, lane, 2 + g);
+                else
+                    pair_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
+                                    val_row, ms->hist[g], ms->xch[g], part, lane, 2 + g);
+            }
+            // the buffer is free for the epilogue's group after next
+            tc::named_bar_sync(7, kSelThreads);
+            if (stid == 0) tc::mbar_arrive(&ms->sc_empty[b]);
+            ++sc_n;
             if (lane == 0) tc::mbar_arrive(&ms->info_empty[slot]);
         }
     }
@@ -964,7 +1017,8 @@ cudaError_t launch_di(const IndexerArgs &a, int hpad, const CUtensorMap &qm, con
 
 int32_t indexer_scratch_rows_threshold() { return kScoreCap; }
 
-int64_t indexer_scratch_floats_per_cta(int32_t Tc) { return (int64_t)kG * Tc; }
+// two score buffers of kG tokens (one being scored, one being selected)
+int64_t indexer_scratch_floats_per_cta(int32_t Tc) { return 2 * (int64_t)kG * Tc; }
 
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t, int32_t, int32_t) {
     if (Tc <= kScoreCap || T <= 0) return 0;
