@@ -24,7 +24,7 @@
 //     sequence (each with its own row range); visibility masks per token.
 //   * The scores of a group go to one of two buffers in shared memory (global
 //     scratch when a sequence offers more than kScoreCap rows). Four
-//     selection warps select the top-k of one group while the four epilogue
+//     selection warps select the top-k of one group while the eight epilogue
 //     warps score the next into the other buffer: each token's selection is
 //     done by two warps (pair_topk), a radix select on order-preserving keys
 //     with 8-bit digits below the bits all of the token's keys share,
@@ -36,8 +36,8 @@
 //     only those go through the pipeline, and the epilogue warps write every
 //     other row (16-byte stores) while the pipeline's loads and first MMAs
 //     run.
-//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-5 epilogue
-//     (one TMEM lane quarter each), 6-9 selection. Every mbarrier wait is
+//   * Warp roles: 0 producer (TMA), 1 tensor memory + MMA issue, 2-9 epilogue
+//     (TMEM lane quarter x token), 10-13 selection. Every mbarrier wait is
 //     bounded.
 #include "common.cuh"
 #include "internal.h"
@@ -48,8 +48,8 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 320;   // producer, MMA, 4 epilogue warps, 4 selection warps
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 448;   // producer, MMA, 8 epilogue warps, 4 selection warps
+constexpr int kEpiThreads = 256;
 constexpr int kSelThreads = 128;
 constexpr int kG = 2;               // tokens per group
 constexpr int kStagesA = 3;         // k tile stages
@@ -513,7 +513,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         }
         for (int i = 0; i < kInfoSlots; ++i) {
             tc::mbar_init(&ms->info_full[i], 1);
-            tc::mbar_init(&ms->info_empty[i], 9);  // the MMA thread, 4 epilogue and 4 selection warps
+            tc::mbar_init(&ms->info_empty[i], 13);  // the MMA thread, 8 epilogue and 4 selection warps
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&ms->sc_full[i], 1);
@@ -577,14 +577,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
     tc::tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
 
-    // Rows of the groups with nothing to score, written by the eight epilogue
+    // Rows of the groups with nothing to score, written by the twelve epilogue
     // and selection warps first (while the producer and the MMA warp start on
     // the scored groups): 32 tokens found at a time per warp, one row per warp
     // store round (16-byte stores when aligned).
     auto bulk_fill = [&]() {
         if (!bulk) return;
         const bool vec = (a.topk & 3) == 0 && (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
-        for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += 256) {
+        for (int64_t base = 32 * (warp - 2); base < my_groups * kG; base += 384) {
             const int64_t li = base + lane;
             const int64_t k = li / kG;
             int32_t t = -1, n = 0, cb = 0;
@@ -716,6 +716,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 }
                 continue;
             }
+            // Start the group's q rows and its first k tile towards L2 while
+            // the buffers they go to are still in use.
+            if (lane == 0) {
+                const int32_t nt = min(kG, a.T - gi.t0);
+                tc::prefetch_l2_bulk(a.q + (int64_t)gi.t0 * a.Hi * DI, (uint32_t)(nt * a.Hi * DI * 2));
+                const int32_t rows = min(kTileRows, gi.nv[__ffs(gi.pass[0].mask) - 1]);
+                if (rows > 0)
+                    tc::prefetch_l2_bulk(a.k + (int64_t)gi.pass[0].cbase * DI, (uint32_t)(rows * DI * 2));
+            }
             const uint32_t slot = it % kInfoSlots;
             bool ok = cx.wait(&ms->info_empty[slot], ((it / kInfoSlots) & 1) ^ 1, 10);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -817,12 +826,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ================================================== epilogue warps
-        // Warp 2..5: TMEM lane quarter q4 (the warp's own), all N columns.
+        // Warps 2..9: TMEM lane quarter q4 (the warp's own) and token `half`
+        // of the group (its N / 2 columns).
         const int q4 = warp & 3;
         const int row = 32 * q4 + lane;
         const int ltid = tid - 64;
+        const int half = (warp - 2) >> 2;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
         bulk_fill();
@@ -871,37 +882,33 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                     for (int g = 0; g < kG; ++g) acc[g] = 0.0f;
                     if constexpr (HPAD >= 32) {
-                        // 32-column chunks lie inside one token: two chunks per
-                        // tensor-memory wait, weights as float4, two partial
-                        // sums per token
-                        float part[kG][2];
+                        // this token's HPAD columns: all its 32-column chunks
+                        // per tensor-memory wait, weights as float4, two
+                        // partial sums
+                        constexpr int kChunks = HPAD / 32;
+                        float x[kChunks][32];
 #pragma unroll
-                        for (int g = 0; g < kG; ++g) part[g][0] = part[g][1] = 0.0f;
+                        for (int cc = 0; cc < kChunks; ++cc)
+                            tc::tmem_ld32(col0 + HPAD * half + 32 * cc, x[cc]);
+                        tc::tmem_wait_ld();
+                        float part0 = 0.0f, part1 = 0.0f;
 #pragma unroll
-                        for (int cc = 0; cc < N / 32; cc += 2) {
-                            float x[2][32];
-                            tc::tmem_ld32(col0 + 32 * cc, x[0]);
-                            tc::tmem_ld32(col0 + 32 * cc + 32, x[1]);
-                            tc::tmem_wait_ld();
+                        for (int cc = 0; cc < kChunks; ++cc) {
+                            const float4 *wv = reinterpret_cast<const float4 *>(ms->w + half * 64 + 32 * cc);
 #pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const int c0 = 32 * (cc + hh);
-                                const int g = c0 / HPAD, h0 = c0 % HPAD;
-                                const float4 *wv = reinterpret_cast<const float4 *>(ms->w + g * 64 + h0);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float4 w4 = wv[i];
-                                    const float *xi = x[hh] + 4 * i;
-                                    part[g][0] = fmaf(w4.x, fmaxf(xi[0], 0.0f), part[g][0]);
-                                    part[g][1] = fmaf(w4.y, fmaxf(xi[1], 0.0f), part[g][1]);
-                                    part[g][0] = fmaf(w4.z, fmaxf(xi[2], 0.0f), part[g][0]);
-                                    part[g][1] = fmaf(w4.w, fmaxf(xi[3], 0.0f), part[g][1]);
-                                }
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 w4 = wv[i];
+                                const float *xi = x[cc] + 4 * i;
+                                part0 = fmaf(w4.x, fmaxf(xi[0], 0.0f), part0);
+                                part1 = fmaf(w4.y, fmaxf(xi[1], 0.0f), part1);
+                                part0 = fmaf(w4.z, fmaxf(xi[2], 0.0f), part0);
+                                part1 = fmaf(w4.w, fmaxf(xi[3], 0.0f), part1);
                             }
                         }
-#pragma unroll
-                        for (int g = 0; g < kG; ++g) acc[g] = part[g][0] + part[g][1];
+                        acc[half] = part0 + part1;
                     } else {
+                        // fewer than 32 heads: all N (<= 32) columns from column
+                        // 0; this warp keeps its token's
 #pragma unroll
                         for (int cc = 0; cc < (N + 31) / 32; ++cc) {
                             float x[32];
@@ -910,9 +917,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 const int col = 32 * cc + i;
-                                if (col < N) {
-                                    const int g = col / HPAD, h = col % HPAD;
-                                    acc[g] = fmaf(ms->w[g * 64 + h], fmaxf(x[i], 0.0f), acc[g]);
+                                if (col < N && col / HPAD == half) {
+                                    const int h = col % HPAD;
+                                    acc[half] = fmaf(ms->w[half * 64 + h], fmaxf(x[i], 0.0f), acc[half]);
                                 }
                             }
                         }
@@ -922,7 +929,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     const int32_t jl = j * kTileRows + row;
 #pragma unroll
                     for (int g = 0; g < kG; ++g)
-                        if (((ps.mask >> g) & 1) && jl < gi.nv[g])
+                        if (g == half && ((ps.mask >> g) & 1) && jl < gi.nv[g])
                             sc[(int64_t)g * sc_stride + jl] = acc[g];
                 }
             }
@@ -937,12 +944,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
         }
     } else {
         // ================================================= selection warps
-        // Warps 6, 7 select token 0 of each group and 8, 9 token 1, one half
-        // of the scores each (pair_topk), while the epilogue scores the next
-        // group into the other buffer.
-        const int sel_tok = (warp - 6) >> 1;
-        const int part = (warp - 6) & 1;
-        const int stid = tid - 192;
+        // Warps 10, 11 select token 0 of each group and 12, 13 token 1, one
+        // half of the scores each (pair_topk), while the epilogue scores the
+        // next group into the other buffer.
+        const int sel_tok = (warp - 10) >> 1;
+        const int part = (warp - 10) & 1;
+        const int stid = tid - 320;
         float *sc_smem = reinterpret_cast<float *>(smem + kOffScore);
         bulk_fill();
         uint32_t it = 0, sc_n = 0;
