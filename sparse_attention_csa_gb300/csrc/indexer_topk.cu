@@ -90,7 +90,7 @@ struct Misc {
     GroupInfo info[kInfoSlots];
     alignas(16) float w[kG * 64];
     int32_t hist[kG][2][256];  // per token: two rounds of packed counts (two warps)
-    uint32_t xch[kG][4];       // per token: the two warps' smallest and largest keys
+    uint32_t keyrange[2][kG][2];  // per score buffer and token: smallest and largest key
     int32_t cu_q[kCuCap + 1], cu_c[kCuCap + 1];  // sequence offsets, when batch <= kCuCap
     uint32_t gscored[kGrpBits / 32];             // this CTA's groups with a token to score
 };
@@ -309,10 +309,9 @@ __device__ void warp_topk(const float *scores, int32_t n, int32_t K, int32_t bas
     }
 }
 
-// The same selection by two warps (part 0 and part 1, on the same scheduler,
-// joined by the 64-thread named barrier `bar`), each sweeping one contiguous
-// half of the scores: the smallest and largest keys are exchanged through
-// `xch`, and each pass's histogram holds both halves' counts packed in one
+// The same selection by two warps (part 0 and part 1, joined by the 64-thread
+// named barrier `bar`), each sweeping one contiguous half of the scores; the
+// smallest and largest keys come from the epilogue, and each pass's histogram holds both halves' counts packed in one
 // word (part 0 in the low 16 bits, part 1 in the high), so that both warps
 // fix the same digit and each also learns how many keys of its own half lie
 // above the bucket and in it. Part 1's first output slot is then part 0's
@@ -325,7 +324,8 @@ constexpr int32_t kPairMax = 130000;
 template <bool kShared>
 __device__ void pair_topk(const float *scores, int32_t n, int32_t K, int32_t base,
                           int32_t *__restrict__ idx_row, float *__restrict__ val_row,
-                          int32_t (*hist)[256], uint32_t *xch, int part, int lane, uint32_t bar) {
+                          int32_t (*hist)[256], uint32_t lo, uint32_t hi, int part, int lane,
+                          uint32_t bar) {
     if (n > kPairMax) {
         if (part == 0) warp_topk<kShared>(scores, n, K, base, idx_row, val_row, hist[0], lane);
         return;
@@ -350,25 +350,8 @@ __device__ void pair_topk(const float *scores, int32_t n, int32_t K, int32_t bas
 #pragma unroll
         for (int m = 0; m < kBatch; ++m) keys[m] = i0 + 32 * m + lane < r1 ? float_key(v[m]) : 0u;
     };
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int32_t i0 = r0; i0 < r1; i0 += kSpan) {
-        load_keys(i0);
-#pragma unroll
-        for (int m = 0; m < kBatch; ++m)
-            if (i0 + 32 * m + lane < r1) {
-                lo = min(lo, keys[m]);
-                hi = max(hi, keys[m]);
-            }
-    }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    if (lane == 0) {
-        xch[2 * part] = lo;
-        xch[2 * part + 1] = hi;
-    }
-    tc::named_bar_sync(bar, 64);
-    lo = min(xch[0], xch[2]);
-    hi = max(xch[1], xch[3]);
+    // lo, hi: the smallest and largest key of all n scores (the epilogue
+    // tracks them while it writes the scores)
     const int free_bits = (lo == hi) ? 0 : 32 - __clz((int)(lo ^ hi));
     uint32_t mask = free_bits == 32 ? 0u : ~((1u << free_bits) - 1u);
     uint32_t prefix = lo & mask;
@@ -859,6 +842,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 sc = sc_smem + b * kG * kScoreCap;
                 sc_stride = kScoreCap;
             }
+            if (ltid < 2 * kG)  // key range of each token, tracked while scoring
+                ms->keyrange[b][ltid >> 1][ltid & 1] = (ltid & 1) ? 0u : 0xffffffffu;
+            uint32_t klo = 0xffffffffu, khi = 0u;
             // weights of the group's tokens (0 beyond Hi / T)
             for (int i = ltid; i < kG * 64; i += kEpiThreads) {
                 const int g = i >> 6, h = i & 63;
@@ -929,13 +915,23 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     const int32_t jl = j * kTileRows + row;
 #pragma unroll
                     for (int g = 0; g < kG; ++g)
-                        if (g == half && ((ps.mask >> g) & 1) && jl < gi.nv[g])
+                        if (g == half && ((ps.mask >> g) & 1) && jl < gi.nv[g]) {
                             sc[(int64_t)g * sc_stride + jl] = acc[g];
+                            const uint32_t u = float_key(acc[g]);
+                            klo = min(klo, u);
+                            khi = max(khi, u);
+                        }
                 }
             }
             if (stop) break;
             // scores complete: hand the buffer to the selection warps (the
             // barrier orders every epilogue thread's writes before the arrive)
+            klo = __reduce_min_sync(0xffffffffu, klo);
+            khi = __reduce_max_sync(0xffffffffu, khi);
+            if (lane == 0) {
+                atomicMin(&ms->keyrange[b][half][0], klo);
+                atomicMax(&ms->keyrange[b][half][1], khi);
+            }
             __threadfence_block();
             tc::named_bar_sync(1, kEpiThreads);
             if (ltid == 0) tc::mbar_arrive(&ms->sc_full[b]);
@@ -977,12 +973,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
                 float *val_row = a.topk_val ? a.topk_val + (int64_t)t * a.topk : nullptr;
                 const int32_t n = gi.valid ? gi.nv[g] : 0;
+                const uint32_t lo = ms->keyrange[b][g][0], hi = ms->keyrange[b][g][1];
                 if (gi.spill)
                     pair_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                     val_row, ms->hist[g], ms->xch[g], part, lane, 2 + g);
+                                     val_row, ms->hist[g], lo, hi, part, lane, 2 + g);
                 else
                     pair_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                    val_row, ms->hist[g], ms->xch[g], part, lane, 2 + g);
+                                    val_row, ms->hist[g], lo, hi, part, lane, 2 + g);
             }
             // the buffer is free for the epilogue's group after next
             tc::named_bar_sync(7, kSelThreads);
