@@ -431,9 +431,10 @@ csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail);
  * makes normal launches give up, which is how the timeout path is tested.
  * Applies to launches made after the call, from any host thread.
  *
- * The device error word's device address is looked up once per device and
- * kept for the process: resetting a device (cudaDeviceReset) while the
- * library is loaded is not supported.
+ * The device addresses of the library's global arrays (the error word, the
+ * no-allocation entry's scratch) are looked up once per device and CUDA
+ * context and kept: after a device reset (cudaDeviceReset), the next call
+ * makes them again for the new context.
  */
 csa_status_t csa_set_wait_limit_ns(uint64_t limit_ns);
 

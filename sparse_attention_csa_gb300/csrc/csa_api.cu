@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "csa.h"
 #include "internal.h"
+#include "tmap.h"
 
 namespace {
 
@@ -16,22 +17,26 @@ __device__ int32_t g_error_word = 0;
 
 constexpr int kMaxDevices = 64;
 int32_t *g_error_ptr[kMaxDevices] = {};
+unsigned long long g_error_ctx[kMaxDevices] = {};  // context the address belongs to
 
-// Device address of g_error_word on the current device (looked up once per
-// device; cudaGetSymbolAddress is the host-side way to name it).
+// Device address of g_error_word on the current device: looked up with
+// cudaGetSymbolAddress (the host-side way to name it) once per device and
+// context, again after a device reset has made a new context.
 int32_t *error_word(csa_status_t *st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *st = CSA_ERR_CUDA;
         return nullptr;
     }
-    if (!g_error_ptr[dev]) {
+    const unsigned long long ctx = csa::current_context_id();
+    if (!g_error_ptr[dev] || ctx == 0 || ctx != g_error_ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
             *st = CSA_ERR_CUDA;
             return nullptr;
         }
         g_error_ptr[dev] = static_cast<int32_t *>(p);
+        g_error_ctx[dev] = csa::current_context_id();
     }
     *st = CSA_OK;
     return g_error_ptr[dev];

@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "csa.h"
 #include "internal.h"
+#include "tmap.h"
 
 namespace {
 
@@ -26,18 +27,22 @@ static __device__ __align__(256) float g_indexer_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
 float *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context the address belongs to
 
 // Device address of g_indexer_scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so it is looked up once per
-// device with cudaGetSymbolAddress (with that device current) and cached.
+// array's name is only a host-side stand-in, so it is looked up with
+// cudaGetSymbolAddress (with that device current) once per device and
+// context, again after a device reset has made a new context.
 csa_status_t scratch_address(float **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA_ERR_CUDA;
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = csa::current_context_id();
+    if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         float *p = nullptr;
         if (cudaGetSymbolAddress((void **)&p, g_indexer_scratch) != cudaSuccess || !p)
             return CSA_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = csa::current_context_id();
     }
     *out = g_scratch_addr[dev];
     return CSA_OK;

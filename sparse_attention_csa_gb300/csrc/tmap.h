@@ -23,6 +23,34 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, through
+// the runtime's driver entry points), or 0 when it cannot be read. A context
+// made after a device reset gets a new id, so host-side caches of device
+// addresses (module globals) key on it.
+inline unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1 = cudaDriverEntryPointSymbolNotFound, r2 = r1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) !=
+                cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
+                cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return 0;
+        get_current = reinterpret_cast<GetCurrent>(p);
+        get_id = reinterpret_cast<GetId>(q);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 // 2-D view [rows, cols] (cols contiguous), box {box_cols, box_rows}.
 inline bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                            uint32_t box_cols, uint32_t box_rows) {
