@@ -74,6 +74,19 @@ __device__ __forceinline__ uint32_t sw_off(uint32_t r, uint32_t u) {
     return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
+// 16-byte copy global -> shared that bypasses registers; `bytes` 0 writes
+// zeros (nothing is read from src then).
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwdArgs a) {
     extern __shared__ unsigned char raw[];
     unsigned char *smem =
@@ -175,37 +188,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
             ms->n_cmp = vis;
         }
         for (int i = tid; i < kTcMaxWin + kTcMaxList; i += kTcThreads) ms->l1[i] = 0.0f;
-        // q and dout rows of the token (zero past H), swizzled K-major
+        // q and dout rows of the token (zero past H), swizzled K-major, by
+        // cp.async: every thread's 32 copies are in flight at once
         for (int i = tid; i < 64 * 64; i += kTcThreads) {  // (head, 16-byte unit of 64)
             const int h = i >> 6, c = (i >> 3) & 7, u = i & 7;
-            uint4 vq = make_uint4(0, 0, 0, 0), vg = vq;
-            if (h < a.H) {
-                const int64_t o = ((int64_t)t * a.H + h) * 512 + 64 * c + 8 * u;
-                vq = __ldg(reinterpret_cast<const uint4 *>(a.q + o));
-                vg = __ldg(reinterpret_cast<const uint4 *>(a.dout + o));
-            }
-            *reinterpret_cast<uint4 *>(smem + kOffQ + c * 8192 + sw_off(h, u)) = vq;
-            *reinterpret_cast<uint4 *>(smem + kOffG + c * 8192 + sw_off(h, u)) = vg;
+            const int64_t o = ((int64_t)t * a.H + min(h, a.H - 1)) * 512 + 64 * c + 8 * u;
+            const uint32_t bytes = h < a.H ? 16u : 0u;
+            cp_async16_zfill(smem + kOffQ + c * 8192 + sw_off(h, u), a.q + o, bytes);
+            cp_async16_zfill(smem + kOffG + c * 8192 + sw_off(h, u), a.dout + o, bytes);
         }
-        // Dv = dout . out per head (8 heads per warp); lse; the sink's gradient
-        for (int h = warp; h < 64; h += kTcThreads / 32) {
-            float s = 0.0f;
-            if (h < a.H) {
-                const int64_t o = ((int64_t)t * a.H + h) * 512;
-                for (int d = lane; d < 512; d += 32)
-                    s += __bfloat162float(a.dout[o + d]) * __bfloat162float(a.out[o + d]);
+        // Dv = dout . out per head while they land (8 heads per warp, two at a
+        // time, 16 dims per lane in 16-byte loads); lse; the sink's gradient
+        for (int j0 = 0; j0 < 8; j0 += 2) {
+            uint4 gv[2][2], ov[2][2];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int h = warp + 8 * (j0 + jj);
+                const int64_t o = ((int64_t)t * a.H + min(h, a.H - 1)) * 512 + 16 * lane;
+                gv[jj][0] = __ldg(reinterpret_cast<const uint4 *>(a.dout + o));
+                gv[jj][1] = __ldg(reinterpret_cast<const uint4 *>(a.dout + o + 8));
+                ov[jj][0] = __ldg(reinterpret_cast<const uint4 *>(a.out + o));
+                ov[jj][1] = __ldg(reinterpret_cast<const uint4 *>(a.out + o + 8));
             }
-            s = warp_sum(s);
-            if (lane == 0) {
-                const float lse = h < a.H ? a.lse[(int64_t)t * a.H + h] : 0.0f;
-                ms->dv[h] = s;
-                ms->lse[h] = lse;
-                if (h < a.H && a.sinks && a.d_sinks) {
-                    const float sk = __ldg(a.sinks + h);
-                    if (sk != -INFINITY) atomicAdd(a.d_sinks + h, -expf(sk - lse) * s);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int h = warp + 8 * (j0 + jj);
+                float s = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv[jj][k]);
+                    const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov[jj][k]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 gf = __bfloat1622float2(g2[e]), of = __bfloat1622float2(o2[e]);
+                        s = fmaf(gf.x, of.x, s);
+                        s = fmaf(gf.y, of.y, s);
+                    }
+                }
+                s = h < a.H ? warp_sum(s) : 0.0f;
+                if (lane == 0) {
+                    const float lse = h < a.H ? a.lse[(int64_t)t * a.H + h] : 0.0f;
+                    ms->dv[h] = s;
+                    ms->lse[h] = lse;
+                    if (h < a.H && a.sinks && a.d_sinks) {
+                        const float sk = __ldg(a.sinks + h);
+                        if (sk != -INFINITY) atomicAdd(a.d_sinks + h, -expf(sk - lse) * s);
+                    }
                 }
             }
         }
+        cp_async_commit_wait_all();
         __syncthreads();
         const int32_t n_cmp = ms->n_cmp;
         const int32_t n_keys = n_win + n_cmp;
@@ -216,17 +248,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
 
         for (int32_t k0 = 0; k0 < n_keys && ok; k0 += kTcKeys) {
             const int nk = min(kTcKeys, n_keys - k0);
-            // the key tile, swizzled K-major; rows past the last key are zero
+            // the key tile, swizzled K-major, by cp.async (every thread's 16
+            // copies in flight at once); rows past the last key are zero
             for (int i = tid; i < kTcKeys * 64; i += kTcThreads) {
                 const int r = i >> 6, c = (i >> 3) & 7, u = i & 7;
-                uint4 v = make_uint4(0, 0, 0, 0);
+                const __nv_bfloat16 *src = a.ori_kv;
+                uint32_t bytes = 0;
                 if (r < nk) {
                     const int32_t key = k0 + r;
-                    const __nv_bfloat16 *src = key < n_win ? a.ori_kv : a.cmp_kv;
-                    v = __ldg(reinterpret_cast<const uint4 *>(src + key_row(key) * 512 + 64 * c + 8 * u));
+                    src = (key < n_win ? a.ori_kv : a.cmp_kv) + key_row(key) * 512 + 64 * c + 8 * u;
+                    bytes = 16;
                 }
-                *reinterpret_cast<uint4 *>(smem + kOffK + c * 8192 + sw_off(r, u)) = v;
+                cp_async16_zfill(smem + kOffK + c * 8192 + sw_off(r, u), src, bytes);
             }
+            cp_async_commit_wait_all();
             tc::fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
