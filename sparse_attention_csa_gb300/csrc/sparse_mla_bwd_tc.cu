@@ -23,9 +23,10 @@
 //   dkv  = (scale dS^T) q + P^T dout  M=64 keys x N=128 dims, K=64 heads, a
 //                             quarter of the 512 dims at a time
 //                                                      TMEM cols 384..511
-// Each quarter is read out of TMEM into shared memory (the key tile's buffer,
-// free once this tile's dq^T MMAs are done) and added to the fp32 row
-// gradients with coalesced float4 atomics (rows are shared between tokens).
+// Each quarter is read out of TMEM and added to the fp32 row gradients with
+// float4 atomics straight from registers (rows are shared between tokens),
+// while the next quarter's MMAs run; the next key tile's copies go in flight
+// as soon as this tile's dq^T MMAs are done with the key buffer.
 // M=64 accumulators put row r in TMEM lane 32 (r / 16) + r % 16. Every wait is
 // bounded; on a timeout the CTA records the error, drains its MMAs and frees
 // TMEM.
@@ -53,7 +54,6 @@ constexpr uint32_t kOffK = 131072;             // 8 x [64 keys x 128 B]
 constexpr uint32_t kOffP = 196608;             // [64 keys x 128 B] bf16 P
 constexpr uint32_t kOffDS = 204800;            // [64 keys x 128 B] bf16 scale*dS
 constexpr uint32_t kOffMisc = 212992;
-constexpr int kStageStride = 132;  // floats per staged gradient row (16-byte aligned, 2-way banks)
 
 struct TcMisc {
     uint64_t bar;
@@ -246,10 +246,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
             return a.cmp_idx ? ms->rows[key - n_win] : cbase + key - n_win;
         };
 
-        for (int32_t k0 = 0; k0 < n_keys && ok; k0 += kTcKeys) {
+        // the key tile from key k0, swizzled K-major, by cp.async (every
+        // thread's 16 copies in flight at once); rows past the last key are zero
+        auto load_tile = [&](int32_t k0) {
             const int nk = min(kTcKeys, n_keys - k0);
-            // the key tile, swizzled K-major, by cp.async (every thread's 16
-            // copies in flight at once); rows past the last key are zero
             for (int i = tid; i < kTcKeys * 64; i += kTcThreads) {
                 const int r = i >> 6, c = (i >> 3) & 7, u = i & 7;
                 const __nv_bfloat16 *src = a.ori_kv;
@@ -261,6 +261,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                 }
                 cp_async16_zfill(smem + kOffK + c * 8192 + sw_off(r, u), src, bytes);
             }
+        };
+        if (n_keys > 0) load_tile(0);
+        for (int32_t k0 = 0; k0 < n_keys && ok; k0 += kTcKeys) {
+            const int nk = min(kTcKeys, n_keys - k0);
+            // this tile's copies (issued here for the first tile, under the
+            // previous tile's row gradients for the others)
             cp_async_commit_wait_all();
             tc::fence_proxy_async_smem();
             __syncthreads();
@@ -346,35 +352,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                                      tc::desc_add(d_g_mn, 2 * qd * 8192 + kk * 2048), id_dk, 1);
                 }
                 if (!(ok = sync_mma())) break;
-                // rows 16 q4 + lane (lane < 16), dims 128 qd + 64 hf .. + 63, staged
-                float *stage = reinterpret_cast<float *>(smem + kOffK);
+                // the key tile is no longer read (the dq^T MMAs are done): the
+                // next tile's copies go in flight under the row gradients
+                if (qd == 0 && k0 + kTcKeys < n_keys) load_tile(k0 + kTcKeys);
+                // rows 16 q4 + lane (lane < 16), dims 128 qd + 64 hf .. + 63
                 float v0[32], v1[32];
                 tc::tmem_ld32(lane_base + kColDK + 64 * hf, v0);
                 tc::tmem_ld32(lane_base + kColDK + 64 * hf + 32, v1);
                 tc::tmem_wait_ld();
-                if (lane < 16) {
-                    float *row = stage + (16 * q4 + lane) * kStageStride + 64 * hf;
+                tc::tc_fence_before();
+                __syncthreads();  // the quarter's TMEM columns are rewritten next
+                // added to the row's fp32 gradient from registers, while the
+                // next quarter's MMAs run
+                const int r = 16 * q4 + lane;
+                if (lane < 16 && r < nk) {
+                    const int32_t key = k0 + r;
+                    float *dst = (key < n_win ? a.d_ori_kv : a.d_cmp_kv) + key_row(key) * 512 +
+                                 128 * qd + 64 * hf;
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
-                        *reinterpret_cast<float4 *>(row + i) = make_float4(v0[i], v0[i + 1], v0[i + 2], v0[i + 3]);
-                        *reinterpret_cast<float4 *>(row + 32 + i) =
-                            make_float4(v1[i], v1[i + 1], v1[i + 2], v1[i + 3]);
+                        atomicAdd(reinterpret_cast<float4 *>(dst + i),
+                                  make_float4(v0[i], v0[i + 1], v0[i + 2], v0[i + 3]));
+                        atomicAdd(reinterpret_cast<float4 *>(dst + 32 + i),
+                                  make_float4(v1[i], v1[i + 1], v1[i + 2], v1[i + 3]));
                     }
                 }
-                tc::tc_fence_before();
-                __syncthreads();
-                // 64 rows x 32 float4: a warp adds 512 contiguous bytes of one row
-                for (int i = tid; i < kTcKeys * 32; i += kTcThreads) {
-                    const int r = i >> 5, c4 = i & 31;
-                    if (r < nk) {
-                        const int32_t key = k0 + r;
-                        float *dst = (key < n_win ? a.d_ori_kv : a.d_cmp_kv) + key_row(key) * 512 +
-                                     128 * qd + 4 * c4;
-                        atomicAdd(reinterpret_cast<float4 *>(dst),
-                                  *reinterpret_cast<const float4 *>(stage + r * kStageStride + 4 * c4));
-                    }
-                }
-                __syncthreads();  // the stage and the quarter's TMEM columns are rewritten next
             }
         }
         if (!ok) break;
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
             for (int i = tid; i < n_cmp; i += kTcThreads)
                 a.cmp_l1[(int64_t)t * a.topk + ms->slots[i]] = ms->l1[n_win + i] * inv_h;
         tc::tc_fence_before();
-        __syncthreads();  // TMEM, the lists and the staged rows are rewritten next token
+        __syncthreads();  // TMEM and the lists are rewritten by the next token
         tc::tc_fence_after();
     }
     // teardown: every MMA issued has completed before tensor memory is freed
