@@ -46,6 +46,7 @@ constexpr int kTcMaxList = 1024;     // top-k entries kept per token
 constexpr int kTcMaxWin = 1024;      // window rows per token
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDK = 384;
+constexpr float kLog2eBwd = 1.4426950408889634f;
 
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;                  // 8 x [64 heads x 128 B]
@@ -61,7 +62,7 @@ struct TcMisc {
     int32_t n_cmp;
     int32_t abort;
     float dv[64];
-    float lse[64];
+    float lse2[64];  // lse in base 2
     float l1[kTcMaxWin + kTcMaxList];
     int32_t rows[kTcMaxList];
     int32_t slots[kTcMaxList];
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
     const bool use_cmp = a.cmp_kv != nullptr && a.Tc > 0;
     const int32_t W = a.window;
     const float scale = a.softmax_scale;
+    const float c2 = scale * kLog2eBwd;  // P = 2^(c2 s - lse log2 e)
 
     if (tid == 0) {
         tc::mbar_init(&ms->bar, 1);
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                 if (lane == 0) {
                     const float lse = h < a.H ? a.lse[(int64_t)t * a.H + h] : 0.0f;
                     ms->dv[h] = s;
-                    ms->lse[h] = lse;
+                    ms->lse2[h] = lse * kLog2eBwd;
                     if (h < a.H && a.sinks && a.d_sinks) {
                         const float sk = __ldg(a.sinks + h);
                         if (sk != -INFINITY) atomicAdd(a.d_sinks + h, -expf(sk - lse) * s);
@@ -301,11 +303,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                         const int h = 32 * hf + i;
                         float p0 = 0.0f, p1 = 0.0f, d0 = 0.0f, d1 = 0.0f;
                         if (key_ok && h < a.H) {
-                            p0 = expf(scale * sv[i] - ms->lse[h]);
+                            p0 = tc::ex2_approx(fmaf(c2, sv[i], -ms->lse2[h]));
                             d0 = scale * p0 * (pv[i] - ms->dv[h]);
                         }
                         if (key_ok && h + 1 < a.H) {
-                            p1 = expf(scale * sv[i + 1] - ms->lse[h + 1]);
+                            p1 = tc::ex2_approx(fmaf(c2, sv[i + 1], -ms->lse2[h + 1]));
                             d1 = scale * p1 * (pv[i + 1] - ms->dv[h + 1]);
                         }
                         psum += p0 + p1;
