@@ -65,7 +65,7 @@ typedef enum {
     CSA_OK = 0,
     CSA_ERR_NULL = 1,         /* a required pointer is NULL                       */
     CSA_ERR_SHAPE = 2,        /* sizes are negative or inconsistent               */
-    CSA_ERR_UNSUPPORTED = 3,  /* a valid request this build does not implement   */
+    CSA_ERR_UNSUPPORTED = 3,  /* a valid request the library does not implement */
     CSA_ERR_WORKSPACE = 4,    /* workspace too small or misaligned                */
     CSA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed      */
     CSA_ERR_DEVICE_CHECK = 6, /* a kernel met inconsistent device data            */

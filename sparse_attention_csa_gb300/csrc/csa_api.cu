@@ -65,7 +65,7 @@ const char *csa_status_string(csa_status_t status) {
         case CSA_OK: return "CSA_OK";
         case CSA_ERR_NULL: return "CSA_ERR_NULL: a required pointer is NULL";
         case CSA_ERR_SHAPE: return "CSA_ERR_SHAPE: negative or inconsistent sizes";
-        case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: request outside what this build implements";
+        case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: request outside what this library implements";
         case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: workspace too small or misaligned";
         case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA call or launch failed";
         case CSA_ERR_DEVICE_CHECK: return "CSA_ERR_DEVICE_CHECK: a kernel met inconsistent device data";
