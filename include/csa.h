@@ -438,6 +438,17 @@ csa_status_t csa_device_error(csa_stream_t stream, int32_t *detail);
  */
 csa_status_t csa_set_wait_limit_ns(uint64_t limit_ns);
 
+/*
+ * Library control, no counterpart on the pages: the indexer selects each
+ * token's top-k with two warps sharing 16-bit counts, and a token with more
+ * visible rows than a bound (130,000) with one warp alone. `rows` lowers that
+ * bound (0 restores it; values above it are ignored; negative ->
+ * CSA_ERR_SHAPE), so that ordinary inputs run the one-warp path: the results
+ * are the same either way, which is how that path is tested. Applies to
+ * launches made after the call, from any host thread.
+ */
+csa_status_t csa_set_pair_select_rows(int32_t rows);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ __all__ = [
     "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
     "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
     "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "csa_compress_thd",
-    "csa_set_wait_limit_ns", "EXPORTED_SYMBOLS",
+    "csa_set_wait_limit_ns", "csa_set_pair_select_rows", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "csa_sparse_mla_bwd", "csa_device_error", "csa_indexer_topk_noalloc",
     "csa_indexer_kl_loss_grad", "csa_bsnd_mla_workspace_size", "csa_sparse_mla_fwd_bsnd",
     "csa_bsnd_indexer_workspace_size", "csa_indexer_topk_bsnd", "csa_compress_thd",
-    "csa_set_wait_limit_ns",
+    "csa_set_wait_limit_ns", "csa_set_pair_select_rows",
 )
 
 _STATUS = {0: "CSA_OK", 1: "CSA_ERR_NULL", 2: "CSA_ERR_SHAPE", 3: "CSA_ERR_UNSUPPORTED",
@@ -97,11 +97,12 @@ def lib():
         L.csa_compress_thd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                        _i32, _vp, _vp]
         L.csa_set_wait_limit_ns.argtypes = [C.c_uint64]
+        L.csa_set_pair_select_rows.argtypes = [_i32]
         for name in ("csa_compress_cu_seqlens", "csa_window_idx", "csa_indexer_topk",
                      "csa_sparse_mla_fwd", "csa_sparse_mla_bwd", "csa_device_error",
                      "csa_indexer_topk_noalloc", "csa_indexer_kl_loss_grad",
                      "csa_sparse_mla_fwd_bsnd", "csa_indexer_topk_bsnd", "csa_compress_thd",
-                     "csa_set_wait_limit_ns"):
+                     "csa_set_wait_limit_ns", "csa_set_pair_select_rows"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -445,3 +446,9 @@ def csa_set_wait_limit_ns(limit_ns: int) -> None:
     ns (0: the default 2 s). A wait that gives up records CSA_ERR_TIMEOUT in
     the device error word; for testing the timeout path."""
     _check(lib().csa_set_wait_limit_ns(int(limit_ns)), "csa_set_wait_limit_ns")
+
+
+def csa_set_pair_select_rows(rows: int) -> None:
+    """Rows above which the indexer selects a token's top-k with one warp
+    instead of two (0: the default bound); for testing the one-warp path."""
+    _check(lib().csa_set_pair_select_rows(int(rows)), "csa_set_pair_select_rows")

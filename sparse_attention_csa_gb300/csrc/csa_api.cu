@@ -56,6 +56,14 @@ uint64_t pipeline_wait_limit_ns() {
     const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
     return v ? v : 2000000000ull;
 }
+
+// 0: the default (the two-warp selection's own bound).
+std::atomic<int32_t> g_pair_select_rows{0};
+
+int32_t pair_select_max_rows(int32_t bound) {
+    const int32_t v = g_pair_select_rows.load(std::memory_order_relaxed);
+    return v > 0 && v < bound ? v : bound;
+}
 }  // namespace csa
 
 extern "C" {
@@ -349,6 +357,12 @@ csa_status_t csa_compress_thd(const float *kv, const float *score, const float *
 
 csa_status_t csa_set_wait_limit_ns(uint64_t limit_ns) {
     csa::g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return CSA_OK;
+}
+
+csa_status_t csa_set_pair_select_rows(int32_t rows) {
+    if (rows < 0) return CSA_ERR_SHAPE;
+    csa::g_pair_select_rows.store(rows, std::memory_order_relaxed);
     return CSA_OK;
 }
 

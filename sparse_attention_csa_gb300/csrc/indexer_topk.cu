@@ -317,16 +317,16 @@ __device__ void warp_topk(const float *scores, int32_t n, int32_t K, int32_t bas
 // above the bucket and in it. Part 1's first output slot is then part 0's
 // count above the bucket plus the bucket keys part 0 takes, with no further
 // exchange. Two rounds of histograms alternate, so one barrier separates a
-// pass's reads from the next pass's zeroing. Rows of more than kPairMax
-// scores (16-bit counts) go to warp_topk on part 0 alone.
+// pass's reads from the next pass's zeroing. Rows of more than pair_max
+// scores (at most kPairMax: 16-bit counts) go to warp_topk on part 0 alone.
 constexpr int32_t kPairMax = 130000;
 
 template <bool kShared>
 __device__ void pair_topk(const float *scores, int32_t n, int32_t K, int32_t base,
                           int32_t *__restrict__ idx_row, float *__restrict__ val_row,
                           int32_t (*hist)[256], uint32_t lo, uint32_t hi, int part, int lane,
-                          uint32_t bar) {
-    if (n > kPairMax) {
+                          uint32_t bar, int32_t pair_max) {
+    if (n > pair_max) {
         if (part == 0) warp_topk<kShared>(scores, n, K, base, idx_row, val_row, hist[0], lane);
         return;
     }
@@ -976,10 +976,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 const uint32_t lo = ms->keyrange[b][g][0], hi = ms->keyrange[b][g][1];
                 if (gi.spill)
                     pair_topk<false>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                     val_row, ms->hist[g], lo, hi, part, lane, 2 + g);
+                                     val_row, ms->hist[g], lo, hi, part, lane, 2 + g, a.pair_max);
                 else
                     pair_topk<true>(sc + (int64_t)g * sc_stride, n, a.topk, gi.cb[g], idx_row,
-                                    val_row, ms->hist[g], lo, hi, part, lane, 2 + g);
+                                    val_row, ms->hist[g], lo, hi, part, lane, 2 + g, a.pair_max);
             }
             // the buffer is free for the epilogue's group after next
             tc::named_bar_sync(7, kSelThreads);
@@ -1035,6 +1035,7 @@ cudaError_t launch_indexer_topk(const IndexerArgs &args, cudaStream_t stream) {
     if (args.T == 0) return cudaSuccess;
     IndexerArgs a = args;
     a.wait_ns = pipeline_wait_limit_ns();
+    a.pair_max = pair_select_max_rows(kPairMax);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

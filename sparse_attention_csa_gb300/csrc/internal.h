@@ -28,6 +28,7 @@ struct IndexerArgs {
     int32_t T, Tc, Hi, Di, batch, cmp_ratio, topk;
     int32_t max_ctas = 0;    // grid bound when > 0 (scratch sized for that many CTAs)
     uint64_t wait_ns = 2000000000ull;  // limit of a pipeline wait (drains keep 2 s)
+    int32_t pair_max = 130000;         // rows above this are selected by one warp
 };
 
 size_t indexer_workspace_bytes(int32_t T, int32_t Tc, int32_t Hi, int32_t Di, int32_t topk);
@@ -128,5 +129,8 @@ int32_t *device_error_word(csa_status_t *st);
 
 // Limit of the forward kernels' pipeline waits (csa_set_wait_limit_ns).
 uint64_t pipeline_wait_limit_ns();
+// Largest row the indexer's two-warp selection takes (csa_set_pair_select_rows),
+// at most `bound`.
+int32_t pair_select_max_rows(int32_t bound);
 
 }  // namespace csa

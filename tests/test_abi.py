@@ -261,6 +261,15 @@ def test_compress_thd_rejects(L):
     assert call(Tc=0) == 0  # nothing to pool
 
 
+def test_controls(L):
+    """The host-only controls: a negative selection bound is rejected; 0
+    restores the defaults."""
+    assert L.csa_set_pair_select_rows(-1) == 2
+    assert L.csa_set_pair_select_rows(256) == 0
+    assert L.csa_set_pair_select_rows(0) == 0
+    assert L.csa_set_wait_limit_ns(0) == 0
+
+
 def test_product_does_not_import_oracle():
     pkg = os.path.join(ROOT, "sparse_attention_csa_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -126,3 +126,42 @@ def test_spill_path_against_oracle(entry, return_value):
     check_topk(case, gi, ref, tokens=toks, gpu_val=gv)
     # every scored late token keeps K distinct rows of its own sequence, ascending
     assert (gi[toks >= 20480] >= 0).all()
+
+
+@pytest.mark.parametrize("scores", ["shared", "workspace"])
+def test_one_warp_selection(scores):
+    """The one-warp selection (taken for tokens with more visible rows than
+    the two-warp selection's bound) on ordinary inputs, with the bound
+    lowered to 256 rows: rows in shared memory (a ragged pack) and rows in
+    the workspace (a 24,576-token sequence). Outputs equal those of the
+    two-warp selection, and agree with the oracle."""
+    if scores == "shared":
+        layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=64, index_heads=16, index_dim=64)
+        case = layer_cases(custom_spec([1, 3, 700, 5, 2600, 333, 2], heads=1, layers=(layer,),
+                                       seed=113))[0]
+        toks = None
+    else:
+        layer = packs.LayerSpec(cmp_ratio=4, indexer=True, topk=512, index_heads=64,
+                                index_dim=128)
+        case = layer_cases(custom_spec([24576], heads=1, layers=(layer,), seed=97))[0]
+        rng = np.random.default_rng(8)
+        toks = np.unique(np.concatenate([rng.integers(20480, 24576, size=24),
+                                         [24575, 2051, 1100]])).astype(np.int32)
+    d, K = case.d, case.layer.topk
+    cuc = csa.csa_compress_cu_seqlens(case.cu_d, 4)
+    ref_idx, ref_val = csa.csa_indexer_topk(d["q_idx"], d["k_idx"], d["w"], case.cu_d, cuc, 4, K,
+                                            return_value=True)
+    try:
+        csa.csa_set_pair_select_rows(256)
+        idx, val = csa.csa_indexer_topk(d["q_idx"], d["k_idx"], d["w"], case.cu_d, cuc, 4, K,
+                                        return_value=True)
+        torch.cuda.synchronize()
+    finally:
+        csa.csa_set_pair_select_rows(0)
+    assert csa.csa_device_error()[0] == 0
+    assert torch.equal(idx, ref_idx) and torch.equal(val, ref_val)
+    ref = oracle_topk(case, toks)
+    gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+    if toks is not None:
+        gi, gv = gi[toks], gv[toks]
+    check_topk(case, gi, ref, tokens=toks, gpu_val=gv)
