@@ -716,7 +716,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                 tc::mbar_arrive(&ms->info_full[slot]);
             }
             ++it;
-            // q rows of the group (4 tokens x HPAD heads; missing rows read as 0)
+            // q rows of the group (kG tokens x HPAD heads; missing rows read as 0)
             ok = cx.wait(&ms->b_empty, (b_n & 1) ^ 1, 11);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (lane == 0) {
@@ -1047,7 +1047,7 @@ cudaError_t launch_indexer_topk(const IndexerArgs &args, cudaStream_t stream) {
     if (a.max_ctas > 0 && ctas > a.max_ctas) ctas = a.max_ctas;
     const int hpad = a.Hi <= 4 ? 4 : a.Hi <= 8 ? 8 : a.Hi <= 16 ? 16 : a.Hi <= 32 ? 32 : 64;
     CUtensorMap qm, km;
-    // q viewed as [T][Hi][Di]; a box of (64 dims, hpad heads, 4 tokens) zero-fills
+    // q viewed as [T][Hi][Di]; a box of (64 dims, hpad heads, kG tokens) zero-fills
     // heads >= Hi and tokens >= T.
     if (!encode_bf16_3d(&qm, a.q, a.Di, a.Hi, a.T, 64, hpad, kG)) return cudaErrorInvalidValue;
     if (a.Tc > 0) {
