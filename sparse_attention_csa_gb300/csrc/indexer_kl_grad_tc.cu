@@ -152,15 +152,15 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kl_grad_tc_kernel(Indexer
         return ms->abort == 0;
     };
     // the listed rows [r0, r0 + 64) as a swizzled K-major tile (rows past n zero)
+    // (cp.async: every thread's copies in flight at once; rows past n zero)
     auto load_tile = [&](int32_t r0, int32_t n) {
         for (int i = tid; i < kRows * 16; i += kThreads) {  // (row, chunk, 16-byte unit)
             const int r = i >> 4, c = (i >> 3) & 1, u = i & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r0 + r < n)
-                v = __ldg(reinterpret_cast<const uint4 *>(a.k + (int64_t)ms->rows[r0 + r] * 128 +
-                                                          64 * c + 8 * u));
-            *reinterpret_cast<uint4 *>(smem + kOffK + c * 8192 + sw_off(r, u)) = v;
+            const bool in = r0 + r < n;
+            const __nv_bfloat16 *src = in ? a.k + (int64_t)ms->rows[r0 + r] * 128 + 64 * c + 8 * u : a.k;
+            tc::cp_async16_zfill(smem + kOffK + c * 8192 + sw_off(r, u), src, in ? 16u : 0u);
         }
+        tc::cp_async_commit_wait_all();
         tc::fence_proxy_async_smem();
         __syncthreads();
     };
@@ -199,12 +199,12 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kl_grad_tc_kernel(Indexer
         if (tid < 64) ms->w[tid] = tid < a.Hi ? __ldg(a.w + (int64_t)t * a.Hi + tid) : 0.0f;
         for (int i = tid; i < 64 * 16; i += kThreads) {  // (head, chunk, 16-byte unit)
             const int h = i >> 4, c = (i >> 3) & 1, u = i & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (h < a.Hi)
-                v = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.Hi + h) * 128 +
-                                                          64 * c + 8 * u));
-            *reinterpret_cast<uint4 *>(smem + kOffQ + c * 8192 + sw_off(h, u)) = v;
+            const bool in = h < a.Hi;
+            const __nv_bfloat16 *src =
+                in ? a.q + ((int64_t)t * a.Hi + h) * 128 + 64 * c + 8 * u : a.q;
+            tc::cp_async16_zfill(smem + kOffQ + c * 8192 + sw_off(h, u), src, in ? 16u : 0u);
         }
+        tc::cp_async_commit_wait_all();
         __syncthreads();
         const int32_t b = ms->info[0];
 

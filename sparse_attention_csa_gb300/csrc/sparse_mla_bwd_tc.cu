@@ -75,18 +75,6 @@ __device__ __forceinline__ uint32_t sw_off(uint32_t r, uint32_t u) {
     return r * 128u + ((u ^ (r & 7u)) << 4);
 }
 
-// 16-byte copy global -> shared that bypasses registers; `bytes` 0 writes
-// zeros (nothing is read from src then).
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                     (uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwdArgs a) {
     extern __shared__ unsigned char raw[];
@@ -196,8 +184,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
             const int h = i >> 6, c = (i >> 3) & 7, u = i & 7;
             const int64_t o = ((int64_t)t * a.H + min(h, a.H - 1)) * 512 + 64 * c + 8 * u;
             const uint32_t bytes = h < a.H ? 16u : 0u;
-            cp_async16_zfill(smem + kOffQ + c * 8192 + sw_off(h, u), a.q + o, bytes);
-            cp_async16_zfill(smem + kOffG + c * 8192 + sw_off(h, u), a.dout + o, bytes);
+            tc::cp_async16_zfill(smem + kOffQ + c * 8192 + sw_off(h, u), a.q + o, bytes);
+            tc::cp_async16_zfill(smem + kOffG + c * 8192 + sw_off(h, u), a.dout + o, bytes);
         }
         // Dv = dout . out per head while they land (8 heads per warp, two at a
         // time, 16 dims per lane in 16-byte loads); lse; the sink's gradient
@@ -239,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                 }
             }
         }
-        cp_async_commit_wait_all();
+        tc::cp_async_commit_wait_all();
         __syncthreads();
         const int32_t n_cmp = ms->n_cmp;
         const int32_t n_keys = n_win + n_cmp;
@@ -261,7 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
                     src = (key < n_win ? a.ori_kv : a.cmp_kv) + key_row(key) * 512 + 64 * c + 8 * u;
                     bytes = 16;
                 }
-                cp_async16_zfill(smem + kOffK + c * 8192 + sw_off(r, u), src, bytes);
+                tc::cp_async16_zfill(smem + kOffK + c * 8192 + sw_off(r, u), src, bytes);
             }
         };
         if (n_keys > 0) load_tile(0);
@@ -269,7 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_mla_bwd_tc_kernel(MlaBwd
             const int nk = min(kTcKeys, n_keys - k0);
             // this tile's copies (issued here for the first tile, under the
             // previous tile's row gradients for the others)
-            cp_async_commit_wait_all();
+            tc::cp_async_commit_wait_all();
             tc::fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {

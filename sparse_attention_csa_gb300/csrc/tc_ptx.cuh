@@ -169,6 +169,19 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 
 // 2^x on the MUFU unit (flush-to-zero); exact enough for softmax weights.
+// 16-byte copy global -> shared that bypasses registers; `bytes` 0 writes
+// zeros (nothing is read from src then).
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
